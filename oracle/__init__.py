@@ -1,0 +1,196 @@
+"""CPU oracle for the guarded W8A8 linear layer.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline leg (and its ``--impl reference`` arm) import this
+package.  The product library never does, and the two share no code: the
+arithmetic lives in ``w8a8_oracle.c`` (plain scalar C), called here through
+ctypes on numpy arrays.
+
+Definition followed (zhidx article "音视频生成提速54倍！浙大等团队开源联合蒸馏方案
+TurboT2VA", section 01 item 3 "量化策略"): weights INT8 per output channel
+(static), activations INT8 per row (dynamic), INT32 accumulation, scales and
+bias applied once after the full accumulation.  The readings the pages leave
+open are listed in ``w8a8_oracle.c``'s header.
+
+Functions:
+  quantize_rows(A)          -> (q int8 [R,K], s float32 [R])      scalar C
+  gemm_s32(Xq, Wq, rows)    -> int32 [len(rows), N]               scalar C, int64-checked
+  gemm_s32_f64(Xq, Wq)      -> int32 [M, N]                       numpy float64 matmul of the
+                               codes; exact because every partial sum is an integer below 2^53
+  epilogue(acc, sx, sw, b)  -> (y32 float32, y bf16 bits uint16)  scalar C
+  bf16_rne(x float32)       -> uint16 bf16 bits                   scalar C
+  linear(X, Wq, sw, bias)   -> the whole path for chosen rows
+
+bf16 tensors are passed as their raw 16-bit patterns (numpy uint16).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build_oracle
+
+_lib = None
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = build_oracle.build()
+        lib = ctypes.CDLL(path)
+        lib.oracle_quantize_rows_f32.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.oracle_quantize_rows_f32.restype = ctypes.c_int
+        lib.oracle_quantize_rows_bf16.argtypes = [_p, _i64, _i64, _p, _p]
+        lib.oracle_quantize_rows_bf16.restype = ctypes.c_int
+        lib.oracle_gemm_s32.argtypes = [_p, _p, _i64, _i64, _i64, _p, _i64, _p]
+        lib.oracle_gemm_s32.restype = ctypes.c_int64
+        lib.oracle_epilogue.argtypes = [_p, _i64, _i64, _p, _p, _p, _p, _p]
+        lib.oracle_epilogue.restype = None
+        lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
+        lib.oracle_bf16_rne.restype = ctypes.c_uint16
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def quantize_rows(A: np.ndarray, dtype: str = None):
+    """Per-row symmetric INT8 quantisation of A[R, K].
+
+    ``A`` is float32, or uint16 holding bf16 bit patterns (``dtype='bf16'``,
+    the default for uint16 arrays).  Returns (codes int8 [R, K], scales
+    float32 [R]).  Rows whose fp32 absmax/127 is 0 get scale 1 and zero codes.
+    """
+    A = np.ascontiguousarray(A)
+    if A.ndim != 2:
+        raise ValueError("A must be 2-D")
+    R, K = A.shape
+    q = np.empty((R, K), dtype=np.int8)
+    s = np.empty((R,), dtype=np.float32)
+    lib = _load()
+    if A.dtype == np.float32 and dtype in (None, "f32"):
+        rc = lib.oracle_quantize_rows_f32(_ptr(A), R, K, _ptr(q), _ptr(s))
+    elif A.dtype == np.uint16 and dtype in (None, "bf16"):
+        rc = lib.oracle_quantize_rows_bf16(_ptr(A), R, K, _ptr(q), _ptr(s))
+    else:
+        raise TypeError("A must be float32 or uint16 (bf16 bits), got %s" % A.dtype)
+    if rc != 0:
+        raise ValueError("non-finite input: the quantiser is not defined there")
+    return q, s
+
+
+def gemm_s32(Xq: np.ndarray, Wq: np.ndarray, rows=None) -> np.ndarray:
+    """acc[i, n] = sum_k Xq[rows[i], k] * Wq[n, k], in int64, checked to fit INT32."""
+    Xq = np.ascontiguousarray(Xq, dtype=np.int8)
+    Wq = np.ascontiguousarray(Wq, dtype=np.int8)
+    M, K = Xq.shape
+    N, K2 = Wq.shape
+    if K != K2:
+        raise ValueError("K mismatch")
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    acc = np.empty((rows.shape[0], N), dtype=np.int32)
+    over = _load().oracle_gemm_s32(_ptr(Xq), _ptr(Wq), M, N, K, _ptr(rows), rows.shape[0], _ptr(acc))
+    if over != 0:
+        raise OverflowError("%d accumulators (or row indices) outside INT32 / range" % over)
+    return acc
+
+
+def gemm_s32_f64(Xq: np.ndarray, Wq: np.ndarray) -> np.ndarray:
+    """The same accumulators through a float64 matrix product of the codes.
+
+    Every product is at most 127*127 = 16129 and |sum| <= K*16129, far below
+    2^53 for any K the layer accepts, so every partial sum of the BLAS routine
+    is an exactly representable integer and the result is exact whatever order
+    it sums in.  Used for the large configurations; checked against
+    ``gemm_s32`` by the tests.
+    """
+    K = Xq.shape[1]
+    if K * 16129 >= 2 ** 53:
+        raise ValueError("K too large for an exact float64 product")
+    acc = Xq.astype(np.float64) @ Wq.astype(np.float64).T
+    if np.abs(acc).max(initial=0.0) > 2 ** 31 - 1:
+        raise OverflowError("accumulator outside INT32")
+    return acc.astype(np.int32)
+
+
+def epilogue(acc: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias=None):
+    """y32 = ((float)acc * sx[row]) * sw[n] + bias[n] in fp32 steps; Y = bf16_rne(y32).
+
+    ``bias`` is float32 (bf16 biases are widened exactly by the caller with
+    ``bf16_bits_to_f32``) or None.  Returns (y32 float32, Y uint16 bf16 bits).
+    """
+    acc = np.ascontiguousarray(acc, dtype=np.int32)
+    nrows, N = acc.shape
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    if sx.shape != (nrows,) or sw.shape != (N,):
+        raise ValueError("scale shapes")
+    b = None
+    if bias is not None:
+        b = np.ascontiguousarray(bias, dtype=np.float32)
+        if b.shape != (N,):
+            raise ValueError("bias shape")
+    y32 = np.empty((nrows, N), dtype=np.float32)
+    y = np.empty((nrows, N), dtype=np.uint16)
+    _load().oracle_epilogue(_ptr(acc), nrows, N, _ptr(sx), _ptr(sw),
+                            _ptr(b) if b is not None else None, _ptr(y32), _ptr(y))
+    return y32, y
+
+
+def bf16_rne(x) -> np.ndarray:
+    """bf16 round-to-nearest-even of float32 values, as uint16 bit patterns."""
+    x = np.asarray(x, dtype=np.float32)
+    f = _load().oracle_bf16_rne
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float32."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def linear(X: np.ndarray, Wq: np.ndarray, sw: np.ndarray, bias=None, rows=None, exact_f64=False):
+    """The hot path for a set of rows: act quant -> INT32 GEMM -> epilogue.
+
+    X is float32 or uint16 (bf16 bits) [M, K]; Wq int8 [N, K]; sw float32 [N];
+    bias float32 [N] or None.  Returns dict with xq, sx (all rows), acc, y32,
+    y (bf16 bits) for the chosen rows.  ``exact_f64`` takes the float64-matmul
+    accumulator path (same result, faster for large shapes).
+    """
+    xq, sx = quantize_rows(X)
+    if rows is None:
+        rows = np.arange(X.shape[0], dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    if exact_f64:
+        acc = gemm_s32_f64(xq[rows], Wq)
+    else:
+        acc = gemm_s32(xq, Wq, rows)
+    y32, y = epilogue(acc, sx[rows], sw, bias)
+    return {"xq": xq, "sx": sx, "rows": rows, "acc": acc, "y32": y32, "y": y}
+
+
+def ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v|: 2^(floor(log2|v|) - 7) for normal v,
+    and the subnormal spacing 2^-133 below 2^-126."""
+    v = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(v > 0, v, 1.0)))
+    e = np.maximum(e, -126.0)
+    return np.exp2(e - 7.0)
