@@ -1,0 +1,385 @@
+"""Benchmark of the guarded W8A8 linear on B300.
+
+Metric: W8A8 linear TOPS (activation quantisation + INT32-exact GEMM + fused
+epilogue) on the video-branch projection, M=6144, K=N=4096, bf16 inputs with
+1 % outlier columns, on one GPU.  One step = one call of the whole hot path:
+the activation-quantisation kernel and the GEMM+epilogue kernel, through the
+C ABI's two stages (exactly what w8a8_linear runs), inputs resident in HBM,
+L2 flushed (256 MiB written) before every step, each kernel timed with CUDA
+events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C) on the host cores on a
+bounded row sample of the same workload.  Under torchrun (N > 1) every rank
+runs an independent replica of the workload (rows are independent, no
+collective on the data path; "weak" scaling), rank 0 prints the line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import w8a8_workloads as wl  # noqa: E402
+
+METRIC = "W8A8 linear TOPS (quant+GEMM+epilogue) at M=6144,K=N=4096; % INT8 tensor peak"
+UNIT = "TOPS"
+WORKLOAD = "video"
+FLUSH_BYTES = 256 << 20
+
+# Algorithmic bytes per unit, for the rooflines:
+#   quant kernel per activation element: 2 B read (bf16) + 2 B written (bf16 code) ; + 8 B per row (scale)
+#   GEMM per launch: codes A (2 M K) + codes B (2 N K) + sx (4 M) + sw (4 N) + bias (2 N) + Y (2 M N)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reported baseline; also the --impl reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(case, rows: int, X_bits, Wq, sw, bias_f32):
+    """Oracle on the first `rows` rows: act quant + INT32 GEMM + epilogue.
+    Returns (seconds, ops)."""
+    import numpy as np
+
+    import oracle
+    t0 = time.perf_counter()
+    xq, sx = oracle.quantize_rows(X_bits[:rows])
+    acc = oracle.gemm_s32(xq, Wq, np.arange(rows, dtype=np.int64))
+    oracle.epilogue(acc, sx, sw, bias_f32)
+    dt = time.perf_counter() - t0
+    return dt, 2 * rows * case.N * case.K
+
+
+def oracle_inputs(case, X, W, b):
+    import numpy as np
+
+    import oracle
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    Wq, sw = oracle.quantize_rows(u16(W))
+    return u16(X), Wq, sw, oracle.bf16_bits_to_f32(u16(b))
+
+
+def calibrate_rows(case, inputs, target_s: float) -> int:
+    rows = 8
+    dt, _ = oracle_sample(case, rows, *inputs)
+    while dt < target_s / 8 and rows < case.M:
+        rows = min(case.M, rows * 4)
+        dt, _ = oracle_sample(case, rows, *inputs)
+    return max(1, min(case.M, int(rows * target_s / max(dt, 1e-6))))
+
+
+def cpu_baseline(case, X, W, b, target_s=12.0):
+    import oracle
+    inputs = oracle_inputs(case, X, W, b)
+    rows = calibrate_rows(case, inputs, target_s)
+    dt, ops = oracle_sample(case, rows, *inputs)
+    return {"value": ops / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "first %d of %d rows of the %s workload (act quant + INT32 GEMM + epilogue), %.1f s"
+                      % (rows, case.M, case.name, dt)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.destroy_process_group()
+            return
+    import oracle
+    case = wl.CASES[args.workload]
+    X, W, b = wl.make(case)
+    inputs = oracle_inputs(case, X, W, b)
+    per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = calibrate_rows(case, inputs, per_step)
+    for _ in range(args.warmup):
+        oracle_sample(case, rows, *inputs)
+    times = []
+    ops = 0
+    for _ in range(args.steps):
+        dt, ops = oracle_sample(case, rows, *inputs)
+        times.append(dt)
+    ms = statistics.mean(times) * 1e3
+    value = ops / (statistics.mean(times)) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int64 scalar (CPU oracle)", "data": "synthetic",
+        "config": config_dict(case),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "first %d of %d rows per step" % (rows, case.M)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def config_dict(case):
+    return {"workload": "video-branch projection: X bf16 [%d,%d] (1%% outlier columns x20) x W [%d,%d]^T + bias"
+                        % (case.M, case.K, case.N, case.K),
+            "M": case.M, "K": case.K, "N": case.N, "l2": "flushed before every step (256 MiB write)",
+            "weights": "quantised offline (static), not timed"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import w8a8_int8_linear_act_b300 as w8
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = wl.CASES[args.workload]
+    X, W, b = wl.make(case)
+    M, K, N = case.M, case.K, case.N
+    Xd, Wd, bd = X.to(dev), W.to(dev), b.to(dev)
+    Wq, sw = w8.quantize_weight(Wd)
+    Wp = w8.pack_weight(Wq)
+    del Wd
+    ws = torch.empty(w8.workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        w8.linear_quant_stage(Xd, ws, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+        w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)
+        if evs is not None:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, bits_ = w8.read_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d bits %#x after warm-up" % (st, bits_))
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    launches = 2 * args.steps
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    g_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    s_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    step_ms = max_over_ranks(statistics.mean(s_ms), world)
+    gemm_ms = statistics.mean(g_ms)
+    quant_ms = statistics.mean(q_ms)
+    st, bits_ = w8.read_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d bits %#x after timed steps" % (st, bits_))
+
+    # end to end through the public call, host buffers, copies inside the timed region
+    Xh = X.pin_memory()
+    Yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    Xe = torch.empty_like(Xd)
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        Xe.copy_(Xh, non_blocking=True)
+        w8.linear(Xe, Wp, sw, bd, out=Y, workspace=ws)
+        Yh.copy_(Y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        Xe.copy_(Xh, non_blocking=True)
+        w8.linear(Xe, Wp, sw, bd, out=Y, workspace=ws)
+        Yh.copy_(Y, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_step = max_over_ranks(statistics.mean(e2e_ms), world)
+
+    ops = case.ops
+    pk = peaks()
+    gemm_tflops = ops / (gemm_ms * 1e-3) / 1e12
+    quant_bytes = M * K * 2 + M * K * 2 + M * 4
+    gemm_bytes = 2 * M * K + 2 * N * K + 4 * M + 4 * N + 2 * N + 2 * M * N
+    quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
+    clocks = sampler.summary()
+    if rank == 0:
+        base = cpu_baseline(case, X, W, b) if (world == 1 and not args.no_cpu_baseline) else None
+        line = {
+            "metric": METRIC,
+            "value": world * ops / (step_ms * 1e-3) / 1e12,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": step_ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int8 codes x int8 codes -> int32 (exact, on bf16 tcgen05 tensor cores)",
+            "data": "synthetic",
+            "config": config_dict(case),
+            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"], "traffic": None,
+                         "kernel": "gemm_w8a8_tcgen05_kernel (GEMM + fused epilogue)",
+                         "algorithmic_bytes": gemm_bytes, "ms": gemm_ms,
+                         "peak_source": "%s bf16 dense burst (the MMA runs bf16 kind::f16)" % pk["source"]},
+            "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                               "frac": quant_gbs / pk["hbm_gbs"], "ms": quant_ms,
+                               "kernel": "quant_rows_kernel (bf16 codes)", "algorithmic_bytes": quant_bytes},
+            "e2e": {"value": world * ops / (e2e_step * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
+                    "d2h_bytes_per_step": Yh.numel() * Yh.element_size()},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "wall_s_timed": t_wall,
+        }
+        if base is not None:
+            line["cpu_baseline"] = base
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(wl.CASES))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * w8a8.h — C ABI of the guarded W8A8 linear layer on B300 (sm_103a).
+ *
+ * The operation.  The zhidx article "音视频生成提速54倍！浙大等团队开源联合蒸馏方案
+ * TurboT2VA", section 01 item 3 ("量化策略"), gives the linear layers of the
+ * video/audio transformer branches as W8A8: the weight is quantised once,
+ * offline, to INT8 with one scale per output channel; the activation is
+ * quantised on every call to INT8 with one scale per row (token); the product
+ * accumulates in INT32; the scales and the bias are applied once, after the
+ * whole accumulation.  Shapes the fast operator cannot take fall back to the
+ * native BF16 linear.  The paperlayer summary of arXiv 2608.24674, section
+ * "C. Fused Multimodal Transformer Operations", calls this guarded
+ * acceleration by shape with a safe fallback.
+ *
+ * Arithmetic, identical to the CPU oracle the tests compare against:
+ *   s[r]    = fp32(absmax_k |A[r][k]| / 127)            IEEE division
+ *             a row with s == 0 (all zeros, or an fp32 absmax that underflows)
+ *             gets s = 1 and zero codes
+ *   q[r][k] = clamp(round_half_even(fp32(A[r][k] / s[r])), -127, 127)
+ *   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]                exact, INT32
+ *   Y[m][n]   = bf16_rne(((float)acc * sx[m]) * sw[n] + bias[n])
+ *               (each step an fp32 operation rounded to nearest even)
+ *
+ * Conventions for every entry point below.
+ *  - Matrices are row-major with the K dimension contiguous: X [M][K],
+ *    W / Wq / Wp [N][K] (one row per output channel, as in a linear layer's
+ *    weight), Y [M][N].
+ *  - Every pointer argument is DEVICE memory owned by the caller, unless a
+ *    comment says otherwise.  The library allocates nothing, frees nothing
+ *    and never synchronises the stream or the device (except
+ *    w8a8_read_status, which says so).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued on it asynchronously; results are ready when
+ *    the stream reaches that point.  The current CUDA device must be the one
+ *    that owns the pointers.
+ *  - `dtype` arguments take a w8a8_dtype value.
+ *  - Errors are returned as w8a8_status.  On any error other than
+ *    W8A8_ERR_CUDA nothing has been launched.  The library never throws,
+ *    exits, traps or asserts on the device.  Device-side waits are bounded:
+ *    a wait that runs out records W8A8_DEV_* bits in the workspace's status
+ *    word (see w8a8_read_status) and the kernel returns.
+ *  - Alignment: X, W, Wq, Wp, Y, acc, sw, bias and workspace 16-byte
+ *    aligned; sx 4-byte aligned (allocations from cudaMalloc or the PyTorch
+ *    caching allocator satisfy all of these).
+ */
+#ifndef W8A8_H
+#define W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W8A8_API __attribute__((visibility("default")))
+#else
+#define W8A8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W8A8_OK = 0,
+    W8A8_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, unknown dtype value */
+    W8A8_ERR_DTYPE = 2,             /* dtype not accepted by this entry point */
+    W8A8_ERR_ALIGNMENT = 3,         /* a pointer misses the alignment stated above */
+    W8A8_ERR_UNSUPPORTED_SHAPE = 4, /* the shape guard rejects (M, N, K); run the BF16 linear instead */
+    W8A8_ERR_WORKSPACE = 5,         /* workspace NULL or smaller than *_workspace_bytes() */
+    W8A8_ERR_CUDA = 6,              /* a CUDA runtime call or kernel launch failed */
+    W8A8_ERR_TIMEOUT = 7,           /* a device-side wait ran out (from w8a8_read_status) */
+    W8A8_ERR_NO_DEVICE = 8          /* no sm_103 device current */
+} w8a8_status;
+
+typedef enum {
+    W8A8_F32 = 0,
+    W8A8_BF16 = 1
+} w8a8_dtype;
+
+/* Reasons reported by w8a8_shape_supported (bitwise OR). */
+#define W8A8_REASON_M          0x01  /* M < 1 or M > 2^31 - 1 */
+#define W8A8_REASON_N          0x02  /* N < 8, N % 8 != 0 or N > 2^31 - 1 */
+#define W8A8_REASON_K          0x04  /* K < 16 or K % 16 != 0 */
+#define W8A8_REASON_K_RANGE    0x08  /* K > 133144: K * 127^2 could leave INT32 */
+#define W8A8_REASON_X_DTYPE    0x10  /* activation dtype is not F32 or BF16 */
+#define W8A8_REASON_BIAS_DTYPE 0x20  /* bias dtype is not F32 or BF16 */
+
+/* Bits of the device status word (w8a8_read_status). */
+#define W8A8_DEV_TIMEOUT_PRODUCER 0x1  /* TMA producer waited too long for a free stage */
+#define W8A8_DEV_TIMEOUT_MMA      0x2  /* MMA issuer waited too long for data or accumulator space */
+#define W8A8_DEV_TIMEOUT_EPILOGUE 0x4  /* epilogue waited too long for a finished accumulator */
+#define W8A8_DEV_TIMEOUT_TEARDOWN 0x8  /* in-flight copies or MMAs did not finish at exit */
+
+/* Largest K whose worst case |acc| = K * 127 * 127 still fits INT32. */
+#define W8A8_MAX_K 133144
+
+/* ---------------------------------------------------------------------------
+ * Shape guard ("guarded W8A8").  Returns 1 when (M, N, K) with these dtypes
+ * runs on the INT8 path, 0 otherwise; `reason` (may be NULL) receives the
+ * W8A8_REASON_* bits of every failed condition (0 when supported).  Pure host
+ * function: no CUDA call, callable without a GPU.  The conditions are the
+ * kernels' own needs: 16-byte row pitches for the TMA copies of int8 and
+ * bf16 rows (K % 16), 16-byte output vectors (N % 8), an INT32 accumulator
+ * that cannot overflow (K <= W8A8_MAX_K).  The pages name no criteria.
+ * ------------------------------------------------------------------------- */
+W8A8_API int w8a8_shape_supported(int64_t M, int64_t N, int64_t K, int x_dtype, int bias_dtype, int* reason);
+
+/* ---------------------------------------------------------------------------
+ * Static per-output-channel weight quantisation (offline, once per layer).
+ *   W  [N][K] of `w_dtype` (F32 or BF16)       in
+ *   Wq [N][K] int8 codes                        out
+ *   sw [N]    fp32 scales                       out
+ * Needs K % 16 == 0, 1 <= K <= W8A8_MAX_K, N >= 1.
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_quantize_weight(const void* W, int w_dtype, int64_t N, int64_t K,
+                                 int8_t* Wq, float* sw, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Dynamic per-row activation quantisation.
+ *   X  [M][K] of `x_dtype` (F32 or BF16)       in
+ *   Xq [M][K] int8 codes                        out
+ *   sx [M]    fp32 scales                       out
+ * Same arithmetic and limits as w8a8_quantize_weight.  M == 0 (or N == 0
+ * for the weight) is a no-op that returns W8A8_OK; the pointers may then be NULL.
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_quantize_act(const void* X, int x_dtype, int64_t M, int64_t K,
+                              int8_t* Xq, float* sx, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Weight operand for the tensor-core GEMM.  B300 (sm_103a) has no tcgen05
+ * integer MMA, so the GEMM multiplies the INT8 codes carried exactly in bf16
+ * (every integer in [-127, 127] is a bf16 value) and keeps every partial sum
+ * an exact integer (see w8a8_linear).  This converts the static codes once:
+ *   Wq [N][K] int8                              in
+ *   Wp [N][K] bf16 bit patterns (uint16)        out, Wp[n][k] == (bf16)Wq[n][k]
+ * Needs K % 16 == 0.  Wp takes 2 * N * K bytes.
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, uint16_t* Wp, void* stream);
+
+/* Bytes of device workspace w8a8_linear needs for an [M][K] activation:
+ * 1024 bytes of alignment slack, a 1024-byte status block, M fp32 row scales
+ * and the M x K activation codes (as bf16), each placed on a 1024-byte
+ * boundary inside the buffer.  Returns 0 for invalid sizes. */
+W8A8_API size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K);
+
+/* ---------------------------------------------------------------------------
+ * The guarded W8A8 linear: Y = dequant(quant(X) * Wq^T) + bias, in two
+ * kernels on `stream`: (1) per-row activation quantisation into the
+ * workspace, (2) the tcgen05 GEMM with the fused epilogue.
+ *   X    [M][K] of `x_dtype` (F32 or BF16)               in
+ *   Wp   [N][K] packed weight codes (w8a8_pack_weight)   in
+ *   sw   [N]    fp32 weight scales                       in
+ *   bias [N]    of `bias_dtype`, or NULL for no bias     in
+ *   Y    [M][N] bf16 bit patterns                        out
+ *   ws   workspace of >= w8a8_linear_workspace_bytes(M, K) bytes; its
+ *        contents on entry do not matter; on return (stream-ordered) it
+ *        holds the status word, sx and the activation codes.
+ * Shapes the guard rejects return W8A8_ERR_UNSUPPORTED_SHAPE with nothing
+ * launched: the caller runs its BF16 linear for them.
+ * The GEMM accumulates in fp32 tensor memory over K-chunks of at most 1024
+ * (1024 * 127^2 < 2^24, so every partial sum is an exactly representable
+ * integer) and drains each chunk into INT32 registers; the result equals the
+ * exact INT32 accumulator.  Calls sharing one workspace must not overlap.
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_linear(const void* X, int x_dtype, int64_t M, int64_t K,
+                        const uint16_t* Wp, const float* sw, int64_t N,
+                        const void* bias, int bias_dtype,
+                        uint16_t* Y, void* ws, size_t ws_bytes, void* stream);
+
+/* The two halves of w8a8_linear, exposed so that each can be timed or
+ * reused alone.  w8a8_linear(...) == quant_stage(...) then gemm_stage(...)
+ * with the same workspace. */
+W8A8_API w8a8_status w8a8_linear_quant_stage(const void* X, int x_dtype, int64_t M, int64_t K,
+                                    void* ws, size_t ws_bytes, void* stream);
+W8A8_API w8a8_status w8a8_linear_gemm_stage(int64_t M, int64_t K, const uint16_t* Wp, const float* sw,
+                                   int64_t N, const void* bias, int bias_dtype,
+                                   uint16_t* Y, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * INT32 accumulators alone (for checking them bit for bit):
+ *   Xq  [M][K] int8 activation codes            in
+ *   Wp  [N][K] packed weight codes              in
+ *   acc [M][N] int32                            out, acc = Xq * Wq^T exactly
+ *   ws  >= w8a8_linear_workspace_bytes(M, K)
+ * Same guard as w8a8_linear (with x_dtype = BF16, no bias).
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64_t N, int64_t K,
+                          int32_t* acc, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Device status of the last call that used `ws`: synchronises `stream`,
+ * copies the workspace's status word to *device_bits (host pointer) and
+ * returns W8A8_OK when it is 0, W8A8_ERR_TIMEOUT when a bounded device wait
+ * ran out (bits W8A8_DEV_*), W8A8_ERR_CUDA if the copy failed.
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_read_status(const void* ws, void* stream, uint32_t* device_bits);
+
+/* Limit, in nanoseconds, for every device-side wait of later launches from
+ * this process (default 2e9 = 2 s).  Values below 1e6 are raised to 1e6. */
+W8A8_API void w8a8_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook: when `on` is nonzero, later GEMM launches issue no operand
+ * copies, so the MMA and epilogue waits run out after the wait limit and
+ * the status word reports it.  Used only by the failure-detection test. */
+W8A8_API void w8a8_debug_skip_loads(int on);
+
+/* Static text for a status value. */
+W8A8_API const char* w8a8_status_str(int status);
+
+/* Library version, for the binding's load check. */
+W8A8_API int w8a8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_H */

@@ -1,0 +1,102 @@
+"""GPU parity of the per-row quantisation kernel against the CPU oracle:
+codes and scales bit-exact (zhidx TurboT2VA article, section 01 item 3:
+activations per row, weights per output channel, INT8)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w8a8_int8_linear_act_b300 as w8
+import w8a8_workloads as wl
+from helpers import bits
+
+pytestmark = pytest.mark.gpu
+
+
+def check_rows(A: torch.Tensor, dev, weight=False):
+    q_ref, s_ref = oracle.quantize_rows(bits(A))
+    Ad = A.to(dev)
+    q, s = (w8.quantize_weight if weight else w8.quantize_act)(Ad)
+    torch.cuda.synchronize()
+    q = q.cpu().numpy()
+    s = s.cpu().numpy()
+    assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32)), "scales differ"
+    bad = np.argwhere(q != q_ref)
+    assert bad.size == 0, "codes differ at %s" % bad[:5].tolist()
+    return q, s
+
+
+@pytest.mark.parametrize("name", list(wl.CASES))
+def test_act_and_weight_codes_reduced(cuda_device, name):
+    """Every workload's recipe at a reduced M/N (K kept): a few CTAs, ragged row counts."""
+    c = wl.CASES[name]
+    X, W, _ = wl.make(c, M=min(c.M, 77), N=min(c.N, 40))
+    check_rows(X, cuda_device)
+    check_rows(W, cuda_device, weight=True)
+
+
+@pytest.mark.parametrize("name", ["tiny", "video", "mlp_down", "audio_m1001_n8192", "audio_m126_n2048"])
+def test_act_codes_full_size(cuda_device, name):
+    c = wl.CASES[name]
+    X, W, _ = wl.make(c)
+    q, s = check_rows(X, cuda_device)
+    if c.zero_last_row:
+        assert s[-1] == 1.0 and not q[-1].any()
+    check_rows(W, cuda_device, weight=True)
+
+
+@pytest.mark.parametrize("K", [16, 32, 48, 256, 272, 2048, 4096, 8192, 16384, 65536, 70016, 133136])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_codes_many_row_lengths(cuda_device, K, dtype):
+    """Row lengths covering every register-tile variant and the two-pass path."""
+    g = torch.Generator().manual_seed(K)
+    R = 3 if K > 60000 else 9
+    X = torch.randn(R, K, generator=g) * torch.logspace(-3, 3, R).unsqueeze(1)
+    X[0, K // 3] = 40.0
+    check_rows(X.to(dtype), cuda_device)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_lossless_and_ties(cuda_device, dtype):
+    """x = k 2^e (one |k| = 127): codes are k exactly; x = (j + 1/2) 2^e: codes
+    round half to even — the same inputs the oracle's pins use."""
+    codes = torch.arange(-127, 128, dtype=torch.float64)
+    rows = [codes * 2.0 ** e for e in (-10, 0, 7)]
+    half = torch.cat([torch.tensor([127.0]), torch.arange(-127, 127, dtype=torch.float64) + 0.5]) * 2.0 ** -4
+    rows.append(torch.cat([half, torch.zeros(1)]))
+    X = torch.stack([r[:255] for r in rows]).to(torch.float32)
+    X = torch.nn.functional.pad(X, (0, 1)).to(dtype)   # K = 256
+    q, s = check_rows(X, cuda_device)
+    assert (q[0, :255].astype(int) == np.arange(-127, 128)).all()
+    assert s[0] == np.float32(2.0 ** -10)
+
+
+def test_zero_and_denormal_rows(cuda_device):
+    """Zero rows, negative-zero rows and fp32 rows whose scale underflows to 0
+    become zero rows (scale 1); one step larger gives a denormal scale."""
+    tiny = float(np.ldexp(np.float32(1.0), -149))
+    X = torch.zeros(5, 32, dtype=torch.float32)
+    X[1] = -0.0
+    X[2, 3] = tiny * 63
+    X[3, 0] = tiny * 127
+    X[3, 1] = -tiny * 127
+    X[4, 7] = 1e-30
+    q, s = check_rows(X, cuda_device)
+    assert s[0] == 1.0 and s[1] == 1.0 and s[2] == 1.0
+    assert s[3] == np.float32(tiny) and q[3, 0] == 127 and q[3, 1] == -127
+    Xb = X.to(torch.bfloat16)
+    check_rows(Xb, cuda_device)
+
+
+def test_empty_rows_call(cuda_device):
+    """M = 0 is a no-op (nothing launched) for the quantiser."""
+    X = torch.empty((0, 64), dtype=torch.bfloat16, device=cuda_device)
+    q, s = w8.quantize_act(X)
+    assert q.shape == (0, 64) and s.shape == (0,)
+
+
+def test_pack_weight_exact(cuda_device):
+    Wq = wl.random_codes((300, 512), seed=3)
+    Wp = w8.pack_weight(Wq.to(cuda_device))
+    torch.cuda.synchronize()
+    assert torch.equal(Wp.cpu().float(), Wq.float())

@@ -1,0 +1,271 @@
+"""Guarded W8A8 linear layer for B300 (sm_103a): thin Python binding.
+
+Every entry point here marshals torch tensors into the C ABI of
+``libw8a8.so`` (declared in ``include/w8a8.h``) and raises on a non-OK
+status.  All arithmetic runs in the library's CUDA kernels; PyTorch only
+provides device memory and the current stream.  There is no CPU path: if the
+library cannot be loaded, importing the functions fails loudly.
+
+The layer (zhidx TurboT2VA article, section 01 item 3 "量化策略"): the weight
+is quantised once to INT8 per output channel, the activation per row on every
+call, the product accumulates in INT32, and the two scales and the bias are
+applied once after the full accumulation.  Shapes the guard rejects raise
+``UnsupportedShape``; the caller runs its BF16 linear for them.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
+    "quantize_act", "pack_weight", "workspace_bytes", "linear", "linear_quant_stage",
+    "linear_gemm_stage", "gemm_s32", "read_status", "set_wait_limit_ns", "debug_skip_loads",
+    "W8A8Linear", "F32", "BF16", "MAX_K",
+]
+
+F32 = 0
+BF16 = 1
+MAX_K = 133144
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libw8a8.so")
+_lib = None
+
+_STATUS = {
+    0: "OK", 1: "INVALID_ARG", 2: "DTYPE", 3: "ALIGNMENT", 4: "UNSUPPORTED_SHAPE",
+    5: "WORKSPACE", 6: "CUDA", 7: "TIMEOUT", 8: "NO_DEVICE",
+}
+
+REASONS = {
+    0x01: "M", 0x02: "N", 0x04: "K", 0x08: "K_RANGE", 0x10: "X_DTYPE", 0x20: "BIAS_DTYPE",
+}
+
+
+class W8A8Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (what, _STATUS.get(status, status), _load().w8a8_status_str(status).decode()))
+
+
+class UnsupportedShape(W8A8Error):
+    pass
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            "libw8a8.so is not built (expected at %s); run "
+            "`python w8a8_int8_linear_act_b300/build.py` or __graft_entry__.build()" % _LIB_PATH)
+    lib = ctypes.CDLL(_LIB_PATH)
+    p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sigs = {
+        "w8a8_shape_supported": ([i64, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int)], i32),
+        "w8a8_quantize_weight": ([p, i32, i64, i64, p, p, p], i32),
+        "w8a8_quantize_act": ([p, i32, i64, i64, p, p, p], i32),
+        "w8a8_pack_weight": ([p, i64, i64, p, p], i32),
+        "w8a8_linear_workspace_bytes": ([i64, i64], sz),
+        "w8a8_linear": ([p, i32, i64, i64, p, p, i64, p, i32, p, p, sz, p], i32),
+        "w8a8_linear_quant_stage": ([p, i32, i64, i64, p, sz, p], i32),
+        "w8a8_linear_gemm_stage": ([i64, i64, p, p, i64, p, i32, p, p, sz, p], i32),
+        "w8a8_gemm_s32": ([p, p, i64, i64, i64, p, p, sz, p], i32),
+        "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
+        "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
+        "w8a8_debug_skip_loads": ([i32], None),
+        "w8a8_status_str": ([i32], ctypes.c_char_p),
+        "w8a8_version": ([], i32),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def load():
+    """Load libw8a8.so (raises ImportError if it is missing)."""
+    return _load()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("dtype %s not supported (float32 or bfloat16)" % t.dtype)
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        if st == 4:
+            raise UnsupportedShape(st, what)
+        raise W8A8Error(st, what)
+
+
+def _cuda2d(t, name):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous 2-D tensor" % name)
+
+
+def shape_supported(M: int, N: int, K: int, x_dtype=torch.bfloat16, bias_dtype=torch.bfloat16):
+    """(supported, [reason names]) from the library's shape guard (host only)."""
+    r = ctypes.c_int(0)
+    xd = {torch.float32: F32, torch.bfloat16: BF16}.get(x_dtype, 99)
+    bd = {torch.float32: F32, torch.bfloat16: BF16}.get(bias_dtype, 99)
+    ok = _load().w8a8_shape_supported(M, N, K, xd, bd, ctypes.byref(r))
+    return bool(ok), [v for k, v in REASONS.items() if r.value & k]
+
+
+def quantize_weight(W: torch.Tensor, stream=None):
+    """Static per-output-channel quantisation: W [N, K] -> (Wq int8 [N, K], sw float32 [N])."""
+    _cuda2d(W, "W")
+    N, K = W.shape
+    Wq = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    sw = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _check(_load().w8a8_quantize_weight(_ptr(W), _dt(W), N, K, _ptr(Wq), _ptr(sw), _stream(stream)),
+           "w8a8_quantize_weight")
+    return Wq, sw
+
+
+def quantize_act(X: torch.Tensor, stream=None):
+    """Dynamic per-row quantisation: X [M, K] -> (Xq int8 [M, K], sx float32 [M])."""
+    _cuda2d(X, "X")
+    M, K = X.shape
+    Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(_load().w8a8_quantize_act(_ptr(X), _dt(X), M, K, _ptr(Xq), _ptr(sx), _stream(stream)),
+           "w8a8_quantize_act")
+    return Xq, sx
+
+
+def pack_weight(Wq: torch.Tensor, stream=None) -> torch.Tensor:
+    """INT8 codes -> the same integers as bf16 (the tensor-core operand)."""
+    _cuda2d(Wq, "Wq")
+    N, K = Wq.shape
+    Wp = torch.empty((N, K), dtype=torch.bfloat16, device=Wq.device)
+    _check(_load().w8a8_pack_weight(_ptr(Wq), N, K, _ptr(Wp), _stream(stream)), "w8a8_pack_weight")
+    return Wp
+
+
+def workspace_bytes(M: int, K: int) -> int:
+    return int(_load().w8a8_linear_workspace_bytes(M, K))
+
+
+def _workspace(M, K, device, ws):
+    need = workspace_bytes(M, K)
+    if need == 0:
+        raise UnsupportedShape(4, "workspace size")
+    if ws is None:
+        ws = torch.empty((need,), dtype=torch.uint8, device=device)
+    elif ws.numel() * ws.element_size() < need:
+        raise W8A8Error(5, "workspace")
+    return ws
+
+
+def linear(X: torch.Tensor, Wp: torch.Tensor, sw: torch.Tensor, bias=None, out=None, workspace=None,
+           stream=None) -> torch.Tensor:
+    """Y [M, N] bf16 = W8A8 linear of X [M, K] with packed weight Wp [N, K] and scales sw [N]."""
+    _cuda2d(X, "X")
+    _cuda2d(Wp, "Wp")
+    M, K = X.shape
+    N = Wp.shape[0]
+    if Wp.shape[1] != K:
+        raise ValueError("K mismatch: X %s, Wp %s" % (tuple(X.shape), tuple(Wp.shape)))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = _workspace(M, K, X.device, workspace)
+    bdt = _dt(bias) if bias is not None else BF16
+    _check(_load().w8a8_linear(_ptr(X), _dt(X), M, K, _ptr(Wp), _ptr(sw), N, _ptr(bias), bdt, _ptr(out),
+                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "w8a8_linear")
+    return out
+
+
+def linear_quant_stage(X: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """First half of ``linear``: activation codes and row scales into the workspace."""
+    _cuda2d(X, "X")
+    M, K = X.shape
+    _check(_load().w8a8_linear_quant_stage(_ptr(X), _dt(X), M, K, _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)),
+           "w8a8_linear_quant_stage")
+
+
+def linear_gemm_stage(M: int, K: int, Wp: torch.Tensor, sw: torch.Tensor, bias, out: torch.Tensor,
+                      workspace: torch.Tensor, stream=None):
+    """Second half of ``linear``: GEMM and epilogue from the workspace's codes."""
+    N = Wp.shape[0]
+    bdt = _dt(bias) if bias is not None else BF16
+    _check(_load().w8a8_linear_gemm_stage(M, K, _ptr(Wp), _ptr(sw), N, _ptr(bias), bdt, _ptr(out),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream)), "w8a8_linear_gemm_stage")
+
+
+def gemm_s32(Xq: torch.Tensor, Wp: torch.Tensor, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """acc [M, N] int32 = Xq [M, K] (int8) x Wq^T, from the packed weight Wp [N, K]."""
+    _cuda2d(Xq, "Xq")
+    _cuda2d(Wp, "Wp")
+    M, K = Xq.shape
+    N = Wp.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=Xq.device)
+    ws = _workspace(M, K, Xq.device, workspace)
+    _check(_load().w8a8_gemm_s32(_ptr(Xq), _ptr(Wp), M, N, K, _ptr(out), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream)), "w8a8_gemm_s32")
+    return out
+
+
+def read_status(workspace: torch.Tensor, stream=None):
+    """(status, device bits) of the last call that used this workspace (synchronises the stream)."""
+    bits = ctypes.c_uint32(0)
+    st = _load().w8a8_read_status(_ptr(workspace), _stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def set_wait_limit_ns(ns: int):
+    _load().w8a8_set_wait_limit_ns(int(ns))
+
+
+def debug_skip_loads(on: bool):
+    _load().w8a8_debug_skip_loads(1 if on else 0)
+
+
+class W8A8Linear:
+    """A linear layer with static INT8 weights: quantises W once, then
+    ``layer(X)`` runs the guarded W8A8 path (activation quantisation, tensor-core
+    INT32-exact GEMM, fused dequantisation + bias + bf16 store)."""
+
+    def __init__(self, weight: torch.Tensor, bias=None):
+        self.Wq, self.sw = quantize_weight(weight)
+        self.Wp = pack_weight(self.Wq)
+        self.bias = bias
+        self.out_features, self.in_features = weight.shape
+        self._ws = None
+
+    def supported(self, M: int, x_dtype=torch.bfloat16) -> bool:
+        bdt = self.bias.dtype if self.bias is not None else torch.bfloat16
+        return shape_supported(M, self.out_features, self.in_features, x_dtype, bdt)[0]
+
+    def __call__(self, X: torch.Tensor, out=None) -> torch.Tensor:
+        M, K = X.shape
+        need = workspace_bytes(M, K)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty((need,), dtype=torch.uint8, device=X.device)
+        return linear(X, self.Wp, self.sw, self.bias, out=out, workspace=self._ws)

@@ -1,0 +1,403 @@
+// C ABI of the guarded W8A8 linear layer (declared in include/w8a8.h).
+// Host-side argument checks, the shape guard, tensor-map encoding and kernel
+// launches.  No allocation, no synchronisation (except w8a8_read_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/w8a8.h"
+#include "gemm_tcgen05.cuh"
+#include "quant_rows.cuh"
+
+namespace {
+
+constexpr int kVersion = 1;
+constexpr size_t kAlign = 1024;
+constexpr int kMaxDevices = 64;
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_skip_loads{0};
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    bool gemm_attr_set = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Per-device facts, queried once.  Returns nullptr when the current device
+// cannot run sm_103a code.
+const DeviceInfo* device_info(int* dev_out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaGetLastError();
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        d.ready = true;
+    }
+    if (dev_out) *dev_out = dev;
+    return d.supported ? &d : nullptr;
+}
+
+bool load_encode_fn()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        cudaGetLastError();
+    });
+    return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor [rows][inner] (inner contiguous), tiles of box_rows x 64
+// elements (128 bytes) with 128-byte swizzling, zero fill out of bounds.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t inner, uint32_t box_rows)
+{
+    if (!load_encode_fn()) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2u};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(w8a8::kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Workspace layout, relative to the first 1024-byte boundary at or after the
+// caller's pointer (the caller only guarantees 16 bytes; kAlign bytes of
+// slack are part of the size): status word, row scales, activation codes.
+struct WsLayout {
+    size_t status_off, sx_off, codes_off, total;
+};
+
+bool ws_layout(int64_t M, int64_t K, WsLayout* L)
+{
+    if (M < 1 || K < 1 || M > INT32_MAX || K > INT32_MAX) return false;
+    L->status_off = 0;
+    L->sx_off = kAlign;
+    L->codes_off = L->sx_off + align_up(static_cast<size_t>(M) * 4u, kAlign);
+    L->total = kAlign + L->codes_off + align_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2u, kAlign);
+    return true;
+}
+
+uint8_t* ws_base(const void* ws)
+{
+    return reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(ws), kAlign));
+}
+
+int guard_reasons(int64_t M, int64_t N, int64_t K, int x_dtype, int bias_dtype)
+{
+    int r = 0;
+    if (M < 1 || M > INT32_MAX) r |= W8A8_REASON_M;
+    if (N < 8 || N % 8 != 0 || N > INT32_MAX) r |= W8A8_REASON_N;
+    if (K < 16 || K % 16 != 0) r |= W8A8_REASON_K;
+    if (K > W8A8_MAX_K) r |= W8A8_REASON_K_RANGE;
+    if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) r |= W8A8_REASON_X_DTYPE;
+    if (bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) r |= W8A8_REASON_BIAS_DTYPE;
+    return r;
+}
+
+w8a8_status last_launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- row quant
+
+template <typename TIn, bool kBf16Codes>
+w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* status,
+                               cudaStream_t stream)
+{
+    constexpr int E = w8a8::InVec<TIn>::kElems;
+    const int64_t V = K / E;  // vectors per row
+    // Threads per row: enough that each holds at most 4 vectors, 32..1024.
+    int64_t T = 32;
+    while (T < 1024 && T * 4 < V) T *= 2;
+    const int64_t per = (V + T - 1) / T;
+    const dim3 grid(static_cast<unsigned>(R));
+    const dim3 block(static_cast<unsigned>(T));
+    if (per <= 1)
+        w8a8::quant_rows_kernel<TIn, kBf16Codes, 1><<<grid, block, 0, stream>>>(A, K, Q, S, status);
+    else if (per <= 2)
+        w8a8::quant_rows_kernel<TIn, kBf16Codes, 2><<<grid, block, 0, stream>>>(A, K, Q, S, status);
+    else if (per <= 4)
+        w8a8::quant_rows_kernel<TIn, kBf16Codes, 4><<<grid, block, 0, stream>>>(A, K, Q, S, status);
+    else if (per <= 8)
+        w8a8::quant_rows_kernel<TIn, kBf16Codes, 8><<<grid, block, 0, stream>>>(A, K, Q, S, status);
+    else
+        w8a8::quant_rows_kernel<TIn, kBf16Codes, 0><<<grid, block, 0, stream>>>(A, K, Q, S, status);
+    return last_launch_status();
+}
+
+template <bool kBf16Codes>
+w8a8_status launch_quant(const void* A, int dtype, int64_t R, int64_t K, void* Q, float* S, uint32_t* status,
+                         cudaStream_t stream)
+{
+    if (dtype == W8A8_BF16)
+        return launch_quant_typed<__nv_bfloat16, kBf16Codes>(static_cast<const __nv_bfloat16*>(A), R, K, Q, S,
+                                                             status, stream);
+    return launch_quant_typed<float, kBf16Codes>(static_cast<const float*>(A), R, K, Q, S, status, stream);
+}
+
+w8a8_status check_quant_args(const void* A, int dtype, int64_t R, int64_t K, const void* Q, const float* S)
+{
+    if (R < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (R == 0 && dtype == W8A8_F32) return W8A8_OK;   // empty input: nothing to do, pointers may be NULL
+    if (R == 0 && dtype == W8A8_BF16) return W8A8_OK;
+    if (!A || !Q || !S) return W8A8_ERR_INVALID_ARG;
+    if (dtype != W8A8_F32 && dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (R > INT32_MAX || K < 16 || K % 16 != 0 || K > W8A8_MAX_K) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(A, 16) || !aligned(Q, 16) || !aligned(S, 4)) return W8A8_ERR_ALIGNMENT;
+    return W8A8_OK;
+}
+
+w8a8_status quantize_rows_entry(const void* A, int dtype, int64_t R, int64_t K, int8_t* Q, float* S, void* stream)
+{
+    w8a8_status st = check_quant_args(A, dtype, R, K, Q, S);
+    if (st != W8A8_OK) return st;
+    if (!device_info(nullptr)) return W8A8_ERR_NO_DEVICE;
+    if (R == 0) return W8A8_OK;
+    return launch_quant<false>(A, dtype, R, K, Q, S, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status launch_codes_to_bf16(const int8_t* Qi, uint16_t* Qb, int64_t n, uint32_t* status, int num_sms,
+                                 cudaStream_t stream)
+{
+    const int64_t n16 = n / 16;
+    int64_t blocks = (n16 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    w8a8::codes_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(Qi, Qb, n16, status);
+    return last_launch_status();
+}
+
+// ---------------------------------------------------------------- GEMM
+
+template <bool kOutS32>
+w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t* Wp, int64_t M, int64_t N,
+                        int64_t K, const float* sx, const float* sw, const void* bias, int bias_mode, void* out,
+                        uint32_t* status, cudaStream_t stream)
+{
+    CUtensorMap ta, tb;
+    if (!encode_bf16_2d(&ta, A_codes, M, K, w8a8::kBM)) return W8A8_ERR_CUDA;
+    if (!encode_bf16_2d(&tb, Wp, N, K, w8a8::kBN)) return W8A8_ERR_CUDA;
+    auto kern = w8a8::gemm_w8a8_tcgen05_kernel<kOutS32>;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (!dev->gemm_attr_set) {
+            if (cudaFuncSetAttribute(w8a8::gemm_w8a8_tcgen05_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(w8a8::kGemmSmemBytes)) != cudaSuccess ||
+                cudaFuncSetAttribute(w8a8::gemm_w8a8_tcgen05_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(w8a8::kGemmSmemBytes)) != cudaSuccess) {
+                cudaGetLastError();
+                return W8A8_ERR_CUDA;
+            }
+            dev->gemm_attr_set = true;
+        }
+    }
+    w8a8::GemmParams p;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.kb_per_chunk = w8a8::kMaxKbPerChunk;
+    p.group_m = 8;
+    p.bias_mode = bias_mode;
+    p.sx = sx;
+    p.sw = sw;
+    p.bias = bias;
+    p.out = out;
+    p.status = status;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.skip_loads = g_skip_loads.load();
+    const int64_t tiles = ((M + w8a8::kBM - 1) / w8a8::kBM) * ((N + w8a8::kBN - 1) / w8a8::kBN);
+    const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
+    kern<<<grid, w8a8::kGemmThreads, w8a8::kGemmSmemBytes, stream>>>(ta, tb, p);
+    return last_launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+int w8a8_version(void) { return kVersion; }
+
+const char* w8a8_status_str(int status)
+{
+    switch (status) {
+        case W8A8_OK: return "ok";
+        case W8A8_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or unknown value)";
+        case W8A8_ERR_DTYPE: return "dtype not accepted";
+        case W8A8_ERR_ALIGNMENT: return "pointer not aligned as required";
+        case W8A8_ERR_UNSUPPORTED_SHAPE: return "shape rejected by the W8A8 guard; use the BF16 linear";
+        case W8A8_ERR_WORKSPACE: return "workspace missing or too small";
+        case W8A8_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case W8A8_ERR_TIMEOUT: return "a device-side wait ran out";
+        case W8A8_ERR_NO_DEVICE: return "current CUDA device is not sm_103";
+        default: return "unknown status";
+    }
+}
+
+int w8a8_shape_supported(int64_t M, int64_t N, int64_t K, int x_dtype, int bias_dtype, int* reason)
+{
+    const int r = guard_reasons(M, N, K, x_dtype, bias_dtype);
+    if (reason) *reason = r;
+    return r == 0 ? 1 : 0;
+}
+
+void w8a8_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000000ull ? 1000000ull : ns); }
+
+void w8a8_debug_skip_loads(int on) { g_skip_loads.store(on ? 1 : 0); }
+
+w8a8_status w8a8_quantize_weight(const void* W, int w_dtype, int64_t N, int64_t K, int8_t* Wq, float* sw,
+                                 void* stream)
+{
+    return quantize_rows_entry(W, w_dtype, N, K, Wq, sw, stream);
+}
+
+w8a8_status w8a8_quantize_act(const void* X, int x_dtype, int64_t M, int64_t K, int8_t* Xq, float* sx,
+                              void* stream)
+{
+    return quantize_rows_entry(X, x_dtype, M, K, Xq, sx, stream);
+}
+
+w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, uint16_t* Wp, void* stream)
+{
+    if (!Wq || !Wp || N < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (K % 16 != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(Wq, 16) || !aligned(Wp, 16)) return W8A8_ERR_ALIGNMENT;
+    const DeviceInfo* dev = device_info(nullptr);
+    if (!dev) return W8A8_ERR_NO_DEVICE;
+    if (N == 0 || K == 0) return W8A8_OK;
+    return launch_codes_to_bf16(Wq, Wp, N * K, nullptr, dev->num_sms, static_cast<cudaStream_t>(stream));
+}
+
+size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K)
+{
+    WsLayout L;
+    return ws_layout(M, K, &L) ? L.total : 0;
+}
+
+w8a8_status w8a8_linear_quant_stage(const void* X, int x_dtype, int64_t M, int64_t K, void* ws, size_t ws_bytes,
+                                    void* stream)
+{
+    if (!X || M < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (M < 1 || M > INT32_MAX || K < 16 || K % 16 != 0 || K > W8A8_MAX_K) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    WsLayout L;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(X, 16) || !aligned(ws, 16)) return W8A8_ERR_ALIGNMENT;
+    if (!device_info(nullptr)) return W8A8_ERR_NO_DEVICE;
+    uint8_t* w = ws_base(ws);
+    return launch_quant<true>(X, x_dtype, M, K, w + L.codes_off, reinterpret_cast<float*>(w + L.sx_off),
+                              reinterpret_cast<uint32_t*>(w + L.status_off), static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_linear_gemm_stage(int64_t M, int64_t K, const uint16_t* Wp, const float* sw, int64_t N,
+                                   const void* bias, int bias_dtype, uint16_t* Y, void* ws, size_t ws_bytes,
+                                   void* stream)
+{
+    if (!Wp || !sw || !Y || M < 0 || N < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (bias && bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (guard_reasons(M, N, K, W8A8_BF16, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    WsLayout L;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(Wp, 16) || !aligned(Y, 16) || !aligned(ws, 16) || !aligned(sw, 16)) return W8A8_ERR_ALIGNMENT;
+    if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
+    int devno = 0;
+    DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(&devno));
+    if (!dev) return W8A8_ERR_NO_DEVICE;
+    uint8_t* w = ws_base(ws);
+    const int bias_mode = bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0;
+    return launch_gemm<false>(dev, reinterpret_cast<const uint16_t*>(w + L.codes_off), Wp, M, N, K,
+                              reinterpret_cast<const float*>(w + L.sx_off), sw, bias, bias_mode, Y,
+                              reinterpret_cast<uint32_t*>(w + L.status_off), static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_linear(const void* X, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp, const float* sw,
+                        int64_t N, const void* bias, int bias_dtype, uint16_t* Y, void* ws, size_t ws_bytes,
+                        void* stream)
+{
+    // Validate everything the second stage needs before launching the first.
+    if (!X || !Wp || !sw || !Y || M < 0 || N < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (bias && bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (guard_reasons(M, N, K, x_dtype, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    WsLayout L;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(X, 16) || !aligned(Wp, 16) || !aligned(Y, 16) || !aligned(ws, 16) || !aligned(sw, 16))
+        return W8A8_ERR_ALIGNMENT;
+    if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
+    w8a8_status st = w8a8_linear_quant_stage(X, x_dtype, M, K, ws, ws_bytes, stream);
+    if (st != W8A8_OK) return st;
+    return w8a8_linear_gemm_stage(M, K, Wp, sw, N, bias, bias_dtype, Y, ws, ws_bytes, stream);
+}
+
+w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64_t N, int64_t K, int32_t* acc,
+                          void* ws, size_t ws_bytes, void* stream)
+{
+    if (!Xq || !Wp || !acc || M < 0 || N < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (guard_reasons(M, N, K, W8A8_BF16, W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    WsLayout L;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(Xq, 16) || !aligned(Wp, 16) || !aligned(acc, 16) || !aligned(ws, 16))
+        return W8A8_ERR_ALIGNMENT;
+    int devno = 0;
+    DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(&devno));
+    if (!dev) return W8A8_ERR_NO_DEVICE;
+    uint8_t* w = ws_base(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status_off);
+    uint16_t* codes = reinterpret_cast<uint16_t*>(w + L.codes_off);
+    w8a8_status st = launch_codes_to_bf16(Xq, codes, M * K, status, dev->num_sms, s);
+    if (st != W8A8_OK) return st;
+    return launch_gemm<true>(dev, codes, Wp, M, N, K, nullptr, nullptr, nullptr, 0, acc, status, s);
+}
+
+w8a8_status w8a8_read_status(const void* ws, void* stream, uint32_t* device_bits)
+{
+    if (!ws || !device_bits) return W8A8_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws_base(ws), sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    *device_bits = v;
+    return v == 0 ? W8A8_OK : W8A8_ERR_TIMEOUT;
+}
+
+}  // extern "C"
