@@ -100,3 +100,46 @@ def test_pack_weight_exact(cuda_device):
     Wp = w8.pack_weight(Wq.to(cuda_device))
     torch.cuda.synchronize()
     assert torch.equal(Wp.cpu().float(), Wq.float())
+
+
+def test_near_ties_take_exact_division_f32(cuda_device):
+    """Elements whose quotient x/s lies within 2^-14 of a half-integer (and
+    exactly on it) with a scale that is not a power of two: the kernel must
+    decide them exactly like IEEE division followed by round-half-even."""
+    rng = np.random.default_rng(77)
+    R, K = 64, 1024
+    rows = []
+    for r in range(R):
+        amax = np.float32(rng.uniform(0.3, 30.0))
+        s = np.float32(amax) / np.float32(127.0)
+        k = rng.integers(-127, 127, size=K - 1)
+        delta = rng.choice([0.0, 1e-7, -1e-7, 3e-6, -3e-6, 2.0 ** -15, -2.0 ** -15, 1e-4, -1e-4], size=K - 1)
+        x = ((k + 0.5 + delta) * np.float64(s)).astype(np.float32)
+        rows.append(np.concatenate([[amax], x]).astype(np.float32))
+    X = np.stack(rows)
+    q_ref, s_ref = oracle.quantize_rows(X)
+    v = X.astype(np.float64) / s_ref[:, None].astype(np.float64)
+    near = np.abs(np.abs(v - np.floor(v)) - 0.5) < 2.0 ** -14
+    assert near.sum() > 1000            # the fallback is really exercised
+    check_rows(torch.from_numpy(X), cuda_device)
+
+
+def test_near_ties_bf16(cuda_device):
+    """bf16 rows: exact ties (x = (k + 1/2) 2^e, s = 2^e; every such value has
+    at most 8 significant bits, so it is a bf16 value) and a large random block
+    whose quotients fall near half-integers by chance."""
+    e = -5
+    ks = np.arange(-127, 127) + 0.5
+    tie_row = np.concatenate([[127.0], ks, np.zeros(256 - 1 - ks.size)]) * 2.0 ** e
+    ties = torch.from_numpy(np.tile(tie_row, (8, 1)).astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(ties.float(), torch.from_numpy(np.tile(tie_row, (8, 1)).astype(np.float32)))
+    q, s = check_rows(ties, cuda_device)
+    assert s[0] == np.float32(2.0 ** e)
+    assert list(q[0, 1:5]) == [round(k) for k in ks[:4]]
+    g = torch.Generator().manual_seed(78)
+    Xr = (torch.randn(1024, 2048, generator=g) * torch.rand(1024, 1, generator=g) * 10).to(torch.bfloat16)
+    xb = oracle.bf16_bits_to_f32(bits(Xr)).astype(np.float64)
+    _, s_ref = oracle.quantize_rows(bits(Xr))
+    v = xb / s_ref[:, None]
+    assert (np.abs(np.abs(v - np.floor(v)) - 0.5) < 2.0 ** -14).sum() > 50
+    check_rows(Xr, cuda_device)

@@ -2,9 +2,9 @@
 // item 3 "量化策略": activations per row, dynamically; weights per output
 // channel, statically — both are rows of the operand as stored).
 //
-//   s    = absmax / 127            (IEEE division, __fdiv_rn)
+//   s    = fp32(absmax / 127)      (IEEE division)
 //   s==0 -> zero row: scale 1, codes 0
-//   q    = clamp(rint_half_even(x / s), -127, 127)
+//   q    = clamp(round_half_even(fp32(x / s)), -127, 127)
 //
 // One CTA per row.  The row is read once from HBM with 16-byte vector loads
 // (thread t takes vectors t, t + T, t + 2T, ... so every warp instruction
@@ -14,12 +14,29 @@
 // the register budget take a second pass over the row instead (served from
 // L2).  The codes go out either as int8 (the API's codes) or as bf16 values
 // of the same integers (the tensor-core GEMM's operand).
+//
+// Exact codes without a division per element.  With r = fp32(1/s) (correctly
+// rounded) and v = fp32(x * r), |v - x/s| <= |x/s| * (2^-24 + 2^-24 + 2^-48)
+// <= 2^-16 for |x/s| <= 128, and the fp32 quotient itself is within 2^-18 of
+// x/s, so |v - fp32(x/s)| < 2^-15.  Whenever v is further than 2^-14 from
+// every half-integer, v and fp32(x/s) lie strictly inside the same interval
+// (n - 1/2, n + 1/2) and round to the same integer n.  Only elements closer
+// than that to a tie (about one in 8000 for smooth data), and rows whose
+// reciprocal overflows (s below 2^-128), take the IEEE division.  The
+// rounding to an integer adds 1.5 * 2^23: for |v| < 2^22 the fp32 sum has a
+// unit in the last place of exactly 1, so round-to-nearest-even of the add
+// is round-half-even of v (the classic magic-number rounding).  In the fast
+// path |v| <= 127 * (1 + 2^-20), so no clamp is needed there.
 #pragma once
 
 #include <cstdint>
 #include <cuda_bf16.h>
 
 namespace w8a8 {
+
+constexpr float kRoundMagic = 12582912.0f;            // 1.5 * 2^23
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+constexpr float kNearHalf = 0.5f - 0.00006103515625f; // 0.5 - 2^-14
 
 template <typename TIn>
 struct InVec;
@@ -36,6 +53,20 @@ struct InVec<__nv_bfloat16> {
             f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         }
     }
+    // Largest |x| of the vector folded into a running maximum kept as two
+    // bf16 magnitudes (bit patterns of non-negative floats order like the
+    // values, so an unsigned 16-bit max is exact).
+    __device__ static __forceinline__ void absmax(const uint4& v, uint32_t& m2)
+    {
+        m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+    }
+    __device__ static __forceinline__ float absmax_value(uint32_t m2)
+    {
+        return fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+    }
 };
 
 template <>
@@ -48,25 +79,61 @@ struct InVec<float> {
         f[2] = __uint_as_float(v.z);
         f[3] = __uint_as_float(v.w);
     }
+    __device__ static __forceinline__ void absmax(const uint4& v, uint32_t& m)
+    {
+        m = max(m, v.x & 0x7FFFFFFFu);
+        m = max(m, v.y & 0x7FFFFFFFu);
+        m = max(m, v.z & 0x7FFFFFFFu);
+        m = max(m, v.w & 0x7FFFFFFFu);
+    }
+    __device__ static __forceinline__ float absmax_value(uint32_t m) { return __uint_as_float(m); }
 };
 
-__device__ __forceinline__ int quant_code(float x, float s)
+// Row constants shared by every element of a row.
+struct RowScale {
+    float s;        // scale (1 for a zero row)
+    float r;        // fp32(1 / s)
+    bool zero;      // zero row: all codes 0
+    bool exact;     // reciprocal overflowed: every element takes the division
+};
+
+__device__ __forceinline__ RowScale row_scale(float amax)
 {
-    const int r = __float2int_rn(__fdiv_rn(x, s));  // round to nearest, ties to even
-    return min(127, max(-127, r));
+    RowScale rs;
+    const float s = __fdiv_rn(amax, 127.0f);
+    rs.zero = (s == 0.0f);
+    rs.s = rs.zero ? 1.0f : s;
+    rs.r = __frcp_rn(rs.s);
+    rs.exact = !(fabsf(rs.r) <= 3.402823466e38f);
+    return rs;
 }
 
-// Writes E codes (E = 8 or 4) starting at element offset `e0` of row `row`.
+// The code of x as the fp32 value kRoundMagic + q (q in [-127, 127]).
+__device__ __forceinline__ float code_biased(float x, const RowScale& rs)
+{
+    const float v = __fmul_rn(x, rs.r);
+    float t = __fadd_rn(v, kRoundMagic);
+    const float f = __fsub_rn(v, __fsub_rn(t, kRoundMagic));
+    if (rs.exact || fabsf(f) > kNearHalf) {
+        const float q = __fdiv_rn(x, rs.s);
+        t = __fadd_rn(fminf(fmaxf(q, -127.0f), 127.0f), kRoundMagic);
+    }
+    return rs.zero ? kRoundMagic : t;
+}
+
+// Writes E codes given as biased floats, at element offset `off`.
 template <bool kBf16Codes, int E>
-__device__ __forceinline__ void store_codes(void* Q, int64_t off, const int (&q)[E])
+__device__ __forceinline__ void store_codes(void* Q, int64_t off, const float (&t)[E])
 {
     if constexpr (kBf16Codes) {
+        // bf16 of the integer q is the top half of fp32(q): |q| <= 127 needs
+        // at most 8 significant bits, so the truncation is exact.
         uint32_t w[E / 2];
 #pragma unroll
         for (int i = 0; i < E / 2; ++i) {
-            const uint32_t lo = __bfloat16_as_ushort(__int2bfloat16_rn(q[2 * i]));
-            const uint32_t hi = __bfloat16_as_ushort(__int2bfloat16_rn(q[2 * i + 1]));
-            w[i] = lo | (hi << 16);
+            const float q0 = __fsub_rn(t[2 * i], kRoundMagic);
+            const float q1 = __fsub_rn(t[2 * i + 1], kRoundMagic);
+            w[i] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
         }
         uint16_t* dst = static_cast<uint16_t*>(Q) + off;
         if constexpr (E == 8)
@@ -74,12 +141,15 @@ __device__ __forceinline__ void store_codes(void* Q, int64_t off, const int (&q)
         else
             *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
     } else {
+        // The low byte of bits(kRoundMagic + q) is q's two's-complement byte
+        // (kRoundMagicBits has a zero low byte and |q| < 2^22).
         uint32_t w[E / 4];
 #pragma unroll
-        for (int i = 0; i < E / 4; ++i)
-            w[i] = (static_cast<uint32_t>(q[4 * i]) & 0xFFu) | ((static_cast<uint32_t>(q[4 * i + 1]) & 0xFFu) << 8) |
-                   ((static_cast<uint32_t>(q[4 * i + 2]) & 0xFFu) << 16) |
-                   ((static_cast<uint32_t>(q[4 * i + 3]) & 0xFFu) << 24);
+        for (int i = 0; i < E / 4; ++i) {
+            const uint32_t p01 = __byte_perm(__float_as_uint(t[4 * i]), __float_as_uint(t[4 * i + 1]), 0x0040);
+            const uint32_t p23 = __byte_perm(__float_as_uint(t[4 * i + 2]), __float_as_uint(t[4 * i + 3]), 0x0040);
+            w[i] = __byte_perm(p01, p23, 0x5410);
+        }
         int8_t* dst = static_cast<int8_t*>(Q) + off;
         if constexpr (E == 8)
             *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
@@ -111,6 +181,19 @@ __device__ __forceinline__ float block_max(float v, float* red /* >= 32 floats *
     return m;
 }
 
+template <typename TIn, bool kBf16Codes>
+__device__ __forceinline__ void quantize_vector(const uint4& v, const RowScale& rs, void* Q, int64_t off)
+{
+    using IV = InVec<TIn>;
+    constexpr int E = IV::kElems;
+    float f[E];
+    IV::unpack(v, f);
+    float t[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) t[e] = code_biased(f[e], rs);
+    store_codes<kBf16Codes, E>(Q, off, t);
+}
+
 // NV > 0: each thread keeps up to NV vectors of the row in registers (single
 // HBM read).  NV == 0: two passes over the row (for very long rows).
 // `status`, when not NULL, is cleared by block 0 (start of a linear call).
@@ -131,59 +214,29 @@ __global__ void __launch_bounds__(1024) quant_rows_kernel(const TIn* __restrict_
 
     if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
 
-    float amax = 0.0f;
+    uint32_t m2 = 0;
     if constexpr (NV > 0) {
         uint4 v[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int idx = threadIdx.x + i * T;
-            if (idx < V) v[i] = load_stream(src + idx);
+            v[i] = (idx < V) ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
         }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
+        const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red));
+        if (threadIdx.x == 0) S[row] = rs.s;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int idx = threadIdx.x + i * T;
-            if (idx < V) {
-                float f[E];
-                IV::unpack(v[i], f);
-#pragma unroll
-                for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(f[e]));
-            }
-        }
-        amax = block_max(amax, red);
-        const float s = __fdiv_rn(amax, 127.0f);
-        const bool zero_row = (s == 0.0f);
-        if (threadIdx.x == 0) S[row] = zero_row ? 1.0f : s;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int idx = threadIdx.x + i * T;
-            if (idx < V) {
-                float f[E];
-                IV::unpack(v[i], f);
-                int q[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) q[e] = zero_row ? 0 : quant_code(f[e], s);
-                store_codes<kBf16Codes, E>(Q, out0 + static_cast<int64_t>(idx) * E, q);
-            }
+            if (idx < V) quantize_vector<TIn, kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * E);
         }
     } else {
-        for (int idx = threadIdx.x; idx < V; idx += T) {
-            float f[E];
-            IV::unpack(load_stream(src + idx), f);
-#pragma unroll
-            for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(f[e]));
-        }
-        amax = block_max(amax, red);
-        const float s = __fdiv_rn(amax, 127.0f);
-        const bool zero_row = (s == 0.0f);
-        if (threadIdx.x == 0) S[row] = zero_row ? 1.0f : s;
-        for (int idx = threadIdx.x; idx < V; idx += T) {
-            float f[E];
-            IV::unpack(src[idx], f);
-            int q[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) q[e] = zero_row ? 0 : quant_code(f[e], s);
-            store_codes<kBf16Codes, E>(Q, out0 + static_cast<int64_t>(idx) * E, q);
-        }
+        for (int idx = threadIdx.x; idx < V; idx += T) IV::absmax(load_stream(src + idx), m2);
+        const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red));
+        if (threadIdx.x == 0) S[row] = rs.s;
+        for (int idx = threadIdx.x; idx < V; idx += T)
+            quantize_vector<TIn, kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
     }
 }
 
