@@ -187,6 +187,40 @@ W8A8_API w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t
                           int32_t* acc, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * w8a8_linear for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this entry point exists for this library's users only.
+ *
+ * Who needs it: code that has no way to obtain a device buffer where it calls
+ * the layer — for example a plugin inside an inference runtime that owns the
+ * whole device memory budget and gives its plugins no scratch space, or a
+ * latency-critical path that must not call cudaMalloc (which can synchronise
+ * the device) and has no memory pool to draw from.  Such a caller still owns
+ * X, Wp, sw, bias and Y; only the workspace is taken care of here.
+ *
+ * The workspace is a scratch array built into the library: a file-scope
+ * device array of W8A8_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which
+ * loads the library keeps until the process exits.
+ *  - Arguments, results and the arithmetic are those of w8a8_linear.
+ *  - No cudaMalloc, cudaFree or other allocating call is made.
+ *  - Shapes needing more than the array, w8a8_linear_workspace_bytes(M, K) >
+ *    W8A8_NOALLOC_SCRATCH_BYTES (M * K above about 33.5 million), return
+ *    W8A8_ERR_WORKSPACE with nothing launched.
+ *  - The first call on a device looks up the array's device address
+ *    (once per device, with that device current).  Make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array, and it keeps the previous
+ *    call's contents; what must start at zero is cleared by each call.
+ *    Calls that can overlap on the GPU (different streams, or threads that
+ *    do not order their launches) race on the array: serialise them.
+ *  - The device status word lives in the built-in array, so
+ *    w8a8_read_status cannot be used with this entry point.
+ * ------------------------------------------------------------------------- */
+#define W8A8_NOALLOC_SCRATCH_BYTES (64ull << 20)
+W8A8_API w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K,
+                                         const uint16_t* Wp, const float* sw, int64_t N,
+                                         const void* bias, int bias_dtype, uint16_t* Y, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Device status of the last call that used `ws`: synchronises `stream`,
  * copies the workspace's status word to *device_bits (host pointer) and
  * returns W8A8_OK when it is 0, W8A8_ERR_TIMEOUT when a bounded device wait

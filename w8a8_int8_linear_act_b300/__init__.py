@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
     "quantize_act", "pack_weight", "workspace_bytes", "linear", "linear_quant_stage",
-    "linear_gemm_stage", "gemm_s32", "read_status", "set_wait_limit_ns", "debug_skip_loads",
+    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "read_status", "set_wait_limit_ns", "debug_skip_loads",
     "W8A8Linear", "F32", "BF16", "MAX_K",
 ]
 
@@ -76,6 +76,7 @@ def _load():
         "w8a8_linear_quant_stage": ([p, i32, i64, i64, p, sz, p], i32),
         "w8a8_linear_gemm_stage": ([i64, i64, p, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_gemm_s32": ([p, p, i64, i64, i64, p, p, sz, p], i32),
+        "w8a8_linear_noalloc": ([p, i32, i64, i64, p, p, i64, p, i32, p, p], i32),
         "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "w8a8_debug_skip_loads": ([i32], None),
@@ -229,6 +230,32 @@ def gemm_s32(Xq: torch.Tensor, Wp: torch.Tensor, out=None, workspace=None, strea
     ws = _workspace(M, K, Xq.device, workspace)
     _check(_load().w8a8_gemm_s32(_ptr(Xq), _ptr(Wp), M, N, K, _ptr(out), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)), "w8a8_gemm_s32")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def linear_noalloc(X: torch.Tensor, Wp: torch.Tensor, sw: torch.Tensor, bias=None, out=None,
+                   stream=None) -> torch.Tensor:
+    """``linear`` without a workspace argument, for callers that cannot get
+    device memory at the call site (a plugin whose host runtime owns all device
+    memory, or a path that must not call cudaMalloc).  The library uses its own
+    built-in 64 MiB scratch array; the caller still provides X, Wp, sw, bias
+    and (optionally) Y.  Calls that may overlap on the GPU must be serialised:
+    they share that one array.  Shapes whose workspace would exceed it raise
+    ``W8A8Error`` (WORKSPACE)."""
+    _cuda2d(X, "X")
+    _cuda2d(Wp, "Wp")
+    M, K = X.shape
+    N = Wp.shape[0]
+    if Wp.shape[1] != K:
+        raise ValueError("K mismatch: X %s, Wp %s" % (tuple(X.shape), tuple(Wp.shape)))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    bdt = _dt(bias) if bias is not None else BF16
+    _check(_load().w8a8_linear_noalloc(_ptr(X), _dt(X), M, K, _ptr(Wp), _ptr(sw), N, _ptr(bias), bdt,
+                                       _ptr(out), _stream(stream)), "w8a8_linear_noalloc")
     return out
 
 

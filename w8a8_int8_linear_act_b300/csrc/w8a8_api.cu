@@ -248,6 +248,14 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     return last_launch_status();
 }
 
+// Scratch for w8a8_linear_noalloc: a workspace built into the library for
+// callers that cannot allocate one.  Its device address is looked up once per
+// device (cudaGetSymbolAddress with that device current) and cached here;
+// host code must never use the array's name as a device pointer.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[W8A8_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
 }  // namespace
 
 extern "C" {
@@ -384,6 +392,35 @@ w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64
     w8a8_status st = launch_codes_to_bf16(Xq, codes, M * K, status, dev->num_sms, s);
     if (st != W8A8_OK) return st;
     return launch_gemm<true>(dev, codes, Wp, M, N, K, nullptr, nullptr, nullptr, 0, acc, status, s);
+}
+
+w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp,
+                                const float* sw, int64_t N, const void* bias, int bias_dtype, uint16_t* Y,
+                                void* stream)
+{
+    WsLayout L;
+    if (M < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (ws_layout(M, K, &L) && L.total > W8A8_NOALLOC_SCRATCH_BYTES) return W8A8_ERR_WORKSPACE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return W8A8_ERR_NO_DEVICE;
+    }
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (g_noalloc_ptr[dev] == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+                cudaGetLastError();
+                return W8A8_ERR_CUDA;
+            }
+            g_noalloc_ptr[dev] = p;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return w8a8_linear(X, x_dtype, M, K, Wp, sw, N, bias, bias_dtype, Y, scratch, W8A8_NOALLOC_SCRATCH_BYTES,
+                       stream);
 }
 
 w8a8_status w8a8_read_status(const void* ws, void* stream, uint32_t* device_bits)
