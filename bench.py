@@ -41,6 +41,25 @@ FLUSH_BYTES = 256 << 20
 #   GEMM per launch: codes A (2 M K) + codes B (2 N K) + sx (4 M) + sw (4 N) + bias (2 N) + Y (2 M N)
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM launch
+# on the default workload, from an ncu capture (profiles/gemm_w8a8_tcgen05_*.md).
+# Valid only for the kernel sources it was taken on: the key is a digest of
+# them, and the bench reports null traffic when the sources have changed since.
+GEMM_SOURCES = ["w8a8_int8_linear_act_b300/csrc/gemm_tcgen05.cuh",
+                "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh",
+                "w8a8_int8_linear_act_b300/csrc/w8a8_api.cu"]
+GEMM_TRAFFIC = {"9efacff2cb7441bd": 125.90e6}
+
+
+def sources_digest(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -53,8 +72,9 @@ def peaks():
 
 
 class ClockSampler:
-    """Samples the SM clock and the clock-event (throttle) reasons through NVML
-    every 5 ms while the timed region runs (read-only queries)."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the
+    timed region runs (read-only queries).  NVML first, every 5 ms; if NVML
+    cannot be opened, `nvidia-smi --query-gpu ... -lms 50` in a child process."""
 
     REASONS = {
         "hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
@@ -63,31 +83,58 @@ class ClockSampler:
         "sw_power_cap": "nvmlClocksEventReasonSwPowerCap",
         "hw_power_brake_slowdown": "nvmlClocksEventReasonHwPowerBrakeSlowdown",
     }
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+                  "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+                  "clocks_event_reasons.sw_power_cap"]
 
-    def __init__(self, index: int, period_s: float = 0.005):
+    def __init__(self, index: int, pci_bus_id=None, period_s: float = 0.005):
         self.index = index
+        self.pci = pci_bus_id
         self.period = period_s
         self.samples = []
         self.reasons = set()
         self.max_mhz = None
+        self.source = None
+        self.error = None
         self._stop = threading.Event()
         self._thread = None
         self._nvml = None
+        self._proc = None
 
     def __enter__(self):
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nvml = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            if self.pci:
+                self._h = pynvml.nvmlDeviceGetHandleByPciBusId(self.pci.encode() if isinstance(self.pci, str)
+                                                              else self.pci)
+            else:
+                self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._thread = threading.Thread(target=self._run, daemon=True)
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
             self._thread.start()
-        except Exception:  # no NVML: the line says "unsampled"
+        except Exception as e:  # fall back to nvidia-smi
+            self.error = "nvml: %s: %s" % (type(e).__name__, e)
             self._nvml = None
+            self._start_smi()
         return self
 
-    def _run(self):
+    def _start_smi(self):
+        import subprocess
+        target = self.pci if self.pci else str(self.index)
+        cmd = ["nvidia-smi", "-i", target, "--query-gpu=" + ",".join(self.SMI_FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
+            self._thread = threading.Thread(target=self._run_smi, daemon=True)
+            self._thread.start()
+        except Exception as e:
+            self.error = (self.error or "") + "; nvidia-smi: %s" % e
+
+    def _run_nvml(self):
         nv = self._nvml
         masks = {k: getattr(nv, v) for k, v in self.REASONS.items() if hasattr(nv, v)}
         while not self._stop.is_set():
@@ -97,14 +144,35 @@ class ClockSampler:
                 for name, m in masks.items():
                     if active & m:
                         self.reasons.add(name)
-            except Exception:
-                pass
+            except Exception as e:
+                self.error = "nvml sample: %s" % e
             time.sleep(self.period)
+
+    def _run_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.SMI_FIELDS):
+                continue
+            try:
+                self.samples.append(float(parts[0]))
+                self.max_mhz = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[2:]):
+                if val.lower() == "active":
+                    self.reasons.add(name)
 
     def __exit__(self, *exc):
         self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
         if self._thread is not None:
-            self._thread.join(timeout=2)
+            self._thread.join(timeout=5)
         if self._nvml is not None:
             try:
                 self._nvml.nvmlShutdown()
@@ -114,9 +182,13 @@ class ClockSampler:
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source, "error": self.error}
+        out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+               "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.source}
+        if self.error:
+            out["error"] = self.error
+        return out
 
 
 def dist_env():
@@ -279,7 +351,12 @@ def run_ours(args):
         raise RuntimeError("device status %d bits %#x after warm-up" % (st, bits_))
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index)
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        pci = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+    except Exception:
+        pci = None
+    sampler = ClockSampler(dev.index, pci)
     barrier(world)
     torch.cuda.synchronize()
     with sampler:
@@ -348,7 +425,8 @@ def run_ours(args):
             "data": "synthetic",
             "config": config_dict(case),
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": pk["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"], "traffic": None,
+                         "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
+                         "traffic": GEMM_TRAFFIC.get(sources_digest(GEMM_SOURCES)) if case.name == WORKLOAD else None,
                          "kernel": "gemm_w8a8_tcgen05_kernel (GEMM + fused epilogue)",
                          "algorithmic_bytes": gemm_bytes, "ms": gemm_ms,
                          "peak_source": "%s bf16 dense burst (the MMA runs bf16 kind::f16)" % pk["source"]},
@@ -373,7 +451,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(wl.CASES))
