@@ -48,7 +48,7 @@ FLUSH_BYTES = 256 << 20
 GEMM_SOURCES = ["w8a8_int8_linear_act_b300/csrc/gemm_tcgen05.cuh",
                 "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh",
                 "w8a8_int8_linear_act_b300/csrc/w8a8_api.cu"]
-GEMM_TRAFFIC = {"9efacff2cb7441bd": 125.90e6}
+GEMM_TRAFFIC = {"ea91e8b591ee6ab9": 163.63e6}
 
 
 def sources_digest(paths):
@@ -300,9 +300,21 @@ def run_reference(args):
         dist.destroy_process_group()
 
 
+WORKLOAD_TEXT = {
+    "video": "video-branch projection",
+    "mlp_up": "video-branch MLP up-projection",
+    "mlp_down": "video-branch MLP down-projection",
+    "hires_n4k": "high-resolution video tokens, projection",
+    "hires_n16k": "high-resolution video tokens, MLP up-projection",
+    "tiny": "tiny fp32 layer",
+}
+
+
 def config_dict(case):
-    return {"workload": "video-branch projection: X bf16 [%d,%d] (1%% outlier columns x20) x W [%d,%d]^T + bias"
-                        % (case.M, case.K, case.N, case.K),
+    what = WORKLOAD_TEXT.get(case.name, "audio-branch ragged shape (last row all zero)")
+    dt = "bf16" if case.dtype == torch.bfloat16 else "fp32"
+    extra = " (1% outlier columns x20)" if case.outliers else ""
+    return {"workload": "%s: X %s [%d,%d]%s x W [%d,%d]^T + bias" % (what, dt, case.M, case.K, extra, case.N, case.K),
             "M": case.M, "K": case.K, "N": case.N, "l2": "flushed before every step (256 MiB write)",
             "weights": "quantised offline (static), not timed"}
 
@@ -327,7 +339,7 @@ def run_ours(args):
     Wq, sw = w8.quantize_weight(Wd)
     Wp = w8.pack_weight(Wq)
     del Wd
-    ws = torch.empty(w8.workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+    ws = torch.empty(w8.workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()

@@ -136,11 +136,39 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int x_dtype, int64_t M, in
  * ------------------------------------------------------------------------- */
 W8A8_API w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, uint16_t* Wp, void* stream);
 
-/* Bytes of device workspace w8a8_linear needs for an [M][K] activation:
- * 1024 bytes of alignment slack, a 1024-byte status block, M fp32 row scales
- * and the M x K activation codes (as bf16), each placed on a 1024-byte
- * boundary inside the buffer.  Returns 0 for invalid sizes. */
-W8A8_API size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K);
+/* Workspace sizes for w8a8_linear, w8a8_linear_gemm_stage and w8a8_gemm_s32.
+ *
+ * w8a8_linear_workspace_min_bytes(M, K): the smallest workspace accepted:
+ * 1024 bytes of alignment slack, a 1024-byte header (status word and the
+ * GEMM's split-tile counters), M fp32 row scales and the M x K activation
+ * codes (as bf16), each on a 1024-byte boundary inside the buffer.
+ *
+ * w8a8_linear_workspace_bytes(M, N, K): the minimum plus room for the INT32
+ * partial tiles (128 KB each) of the GEMM's K-split last wave, as planned
+ * for the current device (for a 148-SM device when no device is current).
+ * When the tiles do not fill the SMs evenly, the GEMM cuts the tiles of the
+ * last, partly filled wave along K so that every SM works on it, and adds
+ * the INT32 partials exactly.  A workspace between the two sizes is
+ * accepted; the GEMM then splits only as far as the room allows (results
+ * are identical either way, only the time differs).
+ *
+ * Both return 0 for invalid sizes. */
+W8A8_API size_t w8a8_linear_workspace_min_bytes(int64_t M, int64_t K);
+W8A8_API size_t w8a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* How the GEMM deals its output tiles to the device's SMs, for a workspace
+ * with room for `max_slots` partial tiles of 128 x 256 INT32 (< 0:
+ * unlimited).  For M > 128 a tile is 256 x 256 and runs on a pair of CTAs
+ * on two SMs (one tcgen05 MMA of cta_group::2 for both); otherwise a tile is
+ * 128 x 256 on one CTA.  `num_sms` > 0 plans for that many SMs (pairs:
+ * num_sms / 2); <= 0 plans for the current device as the launch will (148
+ * SMs when none is current).  Writes plan[0] = whole tiles (dealt
+ * round-robin to the workers), plan[1] = K-segments per remaining tile (1 =
+ * no split), plan[2] = K-segment units (remaining tiles x segments, one per
+ * worker), plan[3] = CTAs launched, plan[4] = CTAs per tile (1 or 2).
+ * Returns 1, or 0 for invalid sizes.  Pure host function apart from the
+ * device query; exposed for inspection and tests. */
+W8A8_API int w8a8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t max_slots, int64_t* plan);
 
 /* ---------------------------------------------------------------------------
  * The guarded W8A8 linear: Y = dequant(quant(X) * Wq^T) + bias, in two
@@ -151,9 +179,10 @@ W8A8_API size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K);
  *   sw   [N]    fp32 weight scales                       in
  *   bias [N]    of `bias_dtype`, or NULL for no bias     in
  *   Y    [M][N] bf16 bit patterns                        out
- *   ws   workspace of >= w8a8_linear_workspace_bytes(M, K) bytes; its
- *        contents on entry do not matter; on return (stream-ordered) it
- *        holds the status word, sx and the activation codes.
+ *   ws   workspace of >= w8a8_linear_workspace_min_bytes(M, K) bytes,
+ *        w8a8_linear_workspace_bytes(M, N, K) for full speed; its contents
+ *        on entry do not matter; on return (stream-ordered) it holds the
+ *        status word, sx and the activation codes.
  * Shapes the guard rejects return W8A8_ERR_UNSUPPORTED_SHAPE with nothing
  * launched: the caller runs its BF16 linear for them.
  * The GEMM accumulates in fp32 tensor memory over K-chunks of at most 1024
@@ -180,7 +209,7 @@ W8A8_API w8a8_status w8a8_linear_gemm_stage(int64_t M, int64_t K, const uint16_t
  *   Xq  [M][K] int8 activation codes            in
  *   Wp  [N][K] packed weight codes              in
  *   acc [M][N] int32                            out, acc = Xq * Wq^T exactly
- *   ws  >= w8a8_linear_workspace_bytes(M, K)
+ *   ws  >= w8a8_linear_workspace_min_bytes(M, K) (see w8a8_linear)
  * Same guard as w8a8_linear (with x_dtype = BF16, no bias).
  * ------------------------------------------------------------------------- */
 W8A8_API w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64_t N, int64_t K,
@@ -202,9 +231,11 @@ W8A8_API w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t
  * loads the library keeps until the process exits.
  *  - Arguments, results and the arithmetic are those of w8a8_linear.
  *  - No cudaMalloc, cudaFree or other allocating call is made.
- *  - Shapes needing more than the array, w8a8_linear_workspace_bytes(M, K) >
- *    W8A8_NOALLOC_SCRATCH_BYTES (M * K above about 33.5 million), return
- *    W8A8_ERR_WORKSPACE with nothing launched.
+ *  - Shapes whose smallest workspace does not fit in the array,
+ *    w8a8_linear_workspace_min_bytes(M, K) > W8A8_NOALLOC_SCRATCH_BYTES
+ *    (M * K above about 33.5 million), return W8A8_ERR_WORKSPACE with
+ *    nothing launched.  What the array has beyond that minimum holds the
+ *    GEMM's split partial tiles.
  *  - The first call on a device looks up the array's device address
  *    (once per device, with that device current).  Make that first call
  *    before any stream capture.
@@ -236,6 +267,11 @@ W8A8_API void w8a8_set_wait_limit_ns(uint64_t ns);
  * copies, so the MMA and epilogue waits run out after the wait limit and
  * the status word reports it.  Used only by the failure-detection test. */
 W8A8_API void w8a8_debug_skip_loads(int on);
+
+/* Test hook: when `on` is nonzero, later GEMM launches (and plans) use the
+ * single-CTA form for every M, so that tests can compare both forms on the
+ * same inputs.  Results are identical either way. */
+W8A8_API void w8a8_debug_force_single_cta(int on);
 
 /* Static text for a status value. */
 W8A8_API const char* w8a8_status_str(int status);

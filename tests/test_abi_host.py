@@ -29,7 +29,8 @@ def lib():
 def test_header_declares_the_api():
     names = declared_symbols()
     for required in ("w8a8_quantize_weight", "w8a8_quantize_act", "w8a8_linear", "w8a8_shape_supported",
-                     "w8a8_pack_weight", "w8a8_gemm_s32", "w8a8_linear_workspace_bytes"):
+                     "w8a8_pack_weight", "w8a8_gemm_s32", "w8a8_linear_workspace_bytes",
+                     "w8a8_linear_workspace_min_bytes", "w8a8_gemm_plan"):
         assert required in names
 
 
@@ -82,10 +83,78 @@ def test_guard_dtypes(lib):
     assert not ok and r == ["BIAS_DTYPE"]
 
 
-def test_workspace_bytes(lib):
-    assert w8.workspace_bytes(6144, 4096) == 1024 + 1024 + 6144 * 4 + 6144 * 4096 * 2
-    assert w8.workspace_bytes(126, 2048) == 1024 + 1024 + 1024 + 126 * 2048 * 2
-    assert w8.workspace_bytes(0, 16) == 0
+SLOT = 128 * 256 * 4          # one INT32 partial tile
+
+
+def test_workspace_min_bytes(lib):
+    assert w8.workspace_min_bytes(6144, 4096) == 1024 + 1024 + 6144 * 4 + 6144 * 4096 * 2
+    assert w8.workspace_min_bytes(126, 2048) == 1024 + 1024 + 1024 + 126 * 2048 * 2
+    assert w8.workspace_min_bytes(0, 16) == 0
+
+
+@pytest.mark.parametrize("M,N,K,plan", [
+    # M > 128: 256 x 256 tiles on CTA pairs (74 pairs on 148 SMs).
+    # 384 tiles: 5 full waves, the 14 tiles left are cut in 5 (<= sqrt(64) k-blocks)
+    (6144, 4096, 4096, (370, 5, 70, 148, 2)),
+    (6144, 4096, 16384, (370, 5, 70, 148, 2)),
+    (28672, 4096, 4096, (1776, 4, 64, 148, 2)),        # 1792 tiles, 16 left: 74 // 16 = 4
+    (6144, 16384, 4096, (1536, 1, 0, 148, 2)),         # 56 left > 37: the last wave is mostly full
+    (28672, 16384, 4096, (7168, 1, 0, 148, 2)),
+    (1001, 2048, 2048, (0, 2, 64, 128, 2)),            # 32 tiles on 74 pairs: cut in 2
+    (1001, 8192, 2048, (128, 1, 0, 148, 2)),           # 128 tiles: 54 left > 37
+    (256 * 37, 512, 4096, (74, 1, 0, 148, 2)),         # exactly one wave
+    # M <= 128: 128 x 256 tiles on single CTAs.
+    (126, 2048, 2048, (0, 5, 40, 40, 1)),              # 8 tiles, 32 k-blocks: sqrt caps at 5
+    (126, 8192, 2048, (0, 4, 128, 128, 1)),
+    (64, 128, 256, (0, 2, 2, 2, 1)),                   # 4 k-blocks: at least 2 per segment
+    (64, 128, 64, (1, 1, 0, 1, 1)),                    # one k-block: nothing to split
+])
+def test_gemm_plan_for_workload_shapes(lib, M, N, K, plan):
+    assert w8.gemm_plan(M, N, K, num_sms=148) == plan
+    dp, splits, units, grid, pair = plan
+    assert w8.workspace_bytes(M, N, K) == w8.workspace_min_bytes(M, K) + units * pair * SLOT
+
+
+def test_gemm_plan_single_cta_switch(lib):
+    w8.debug_force_single_cta(True)
+    try:
+        assert w8.gemm_plan(6144, 4096, 4096, num_sms=148) == (740, 5, 140, 148, 1)
+        assert w8.gemm_plan(128 * 37, 1024, 4096, num_sms=148) == (148, 1, 0, 148, 1)
+    finally:
+        w8.debug_force_single_cta(False)
+    assert w8.gemm_plan(6144, 4096, 4096, num_sms=148)[4] == 2
+
+
+def test_gemm_plan_respects_workspace_room(lib):
+    # a pair unit needs two slots (one per CTA)
+    assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=100) == (370, 3, 42, 148, 2)
+    assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=55) == (384, 1, 0, 148, 2)
+    assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=0) == (384, 1, 0, 148, 2)
+    assert w8.gemm_plan(126, 2048, 2048, 148, max_slots=16) == (0, 2, 16, 16, 1)
+
+
+def test_gemm_plan_invariants(lib):
+    """Every tile is either whole or cut into `splits` segments of >= 2
+    k-blocks; the segment units fit the workers; no more than half a wave is
+    cut; CTA pairs exactly when M > 128."""
+    for sms in (148, 132, 8):
+        for M in (1, 127, 128, 129, 1000, 6144, 28672):
+            for N in (8, 256, 264, 2048, 4096, 16384):
+                for K in (16, 64, 128, 1024, 4096, 16384):
+                    dp, s, units, grid, pair = w8.gemm_plan(M, N, K, sms)
+                    assert pair == (2 if M > 128 else 1)
+                    workers = sms // pair
+                    tiles = -(-M // (128 * pair)) * -(-N // 256)
+                    kb = -(-K // 64)
+                    assert grid % pair == 0 and 1 <= grid // pair <= workers
+                    if s == 1:
+                        assert dp == tiles and units == 0 and grid == min(tiles, workers) * pair
+                    else:
+                        rem = tiles - dp
+                        assert rem == tiles % workers and 0 < 2 * rem <= workers
+                        assert units == rem * s <= workers and kb // s >= 2
+                        assert s * s <= kb and rem * pair <= 240
+                        assert grid == (workers if tiles >= workers else units) * pair
 
 
 def test_argument_errors_return_before_any_launch(lib):

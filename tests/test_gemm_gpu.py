@@ -106,3 +106,60 @@ def test_s32_workload_codes_full(cuda_device, name):
     acc = run_gemm(torch.from_numpy(xq), torch.from_numpy(wq), cuda_device)
     ref = oracle.gemm_s32_f64(xq, wq)
     assert np.array_equal(acc, ref), "mismatches: %d" % int((acc != ref).sum())
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (300, 520, 1040),        # 9 tiles on 148 SMs: every tile cut along K
+    (128 * 151, 256, 1024),  # 148 whole tiles, then 3 tiles cut in 4
+    (128, 256, 133136),      # one tile cut into 45 segments of ~46 k-blocks
+])
+def test_s32_k_split_and_whole_tiles_agree(cuda_device, M, N, K):
+    """The K-split of the last wave (INT32 partial tiles added by the last
+    segment to finish) and whole-tile accumulation give the exact INT32
+    accumulator: run once with room for the partial tiles and once with the
+    smallest workspace (no split), both against the oracle."""
+    dev = cuda_device
+    assert w8.gemm_plan(M, N, K)[1] > 1
+    assert w8.gemm_plan(M, N, K, max_slots=0)[1] == 1
+    Xq = wl.random_codes((M, K), seed=M + 3)
+    Wq = wl.random_codes((N, K), seed=N + 4)
+    Wp = w8.pack_weight(Wq.to(dev))
+    Xd = Xq.to(dev)
+    split = w8.gemm_s32(Xd, Wp)
+    ws_min = torch.empty(w8.workspace_min_bytes(M, K), dtype=torch.uint8, device=dev)
+    whole = w8.gemm_s32(Xd, Wp, workspace=ws_min)
+    again = w8.gemm_s32(Xd, Wp)                # a second split launch: same bytes
+    torch.cuda.synchronize()
+    ref = ref_gemm(Xq, Wq)
+    for name, acc in (("split", split), ("whole", whole), ("split again", again)):
+        acc = acc.cpu().numpy()
+        assert np.array_equal(acc, ref), "%s: mismatches %d" % (name, int((acc != ref).sum()))
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (129, 264, 2064),     # one row past a pair's first CTA: the second CTA's rows are all ragged
+    (300, 520, 1040),
+    (1000, 2048, 3200),
+    (2048, 2048, 4096),
+])
+def test_s32_pair_and_single_cta_forms_agree(cuda_device, M, N, K):
+    """The 2-CTA form (256 x 256 tiles, cta_group::2 MMA across two SMs) and
+    the single-CTA form (128 x 256 tiles) on the same codes, both exact."""
+    dev = cuda_device
+    assert w8.gemm_plan(M, N, K)[4] == 2
+    Xq = wl.random_codes((M, K), seed=M + 7)
+    Wq = wl.random_codes((N, K), seed=N + 8)
+    Wp = w8.pack_weight(Wq.to(dev))
+    Xd = Xq.to(dev)
+    pair = w8.gemm_s32(Xd, Wp)
+    w8.debug_force_single_cta(True)
+    try:
+        assert w8.gemm_plan(M, N, K)[4] == 1
+        single = w8.gemm_s32(Xd, Wp)
+    finally:
+        w8.debug_force_single_cta(False)
+    torch.cuda.synchronize()
+    ref = ref_gemm(Xq, Wq)
+    for name, acc in (("pair", pair), ("single", single)):
+        acc = acc.cpu().numpy()
+        assert np.array_equal(acc, ref), "%s: mismatches %d" % (name, int((acc != ref).sum()))

@@ -109,7 +109,7 @@ def test_linear_stages_equal_fused_call(cuda_device):
     Wq, sw = w8.quantize_weight(W.to(cuda_device))
     Wp = w8.pack_weight(Wq)
     Y1 = w8.linear(Xd, Wp, sw, bd)
-    ws = torch.empty(w8.workspace_bytes(256, 1024), dtype=torch.uint8, device=cuda_device)
+    ws = torch.empty(w8.workspace_bytes(256, 512, 1024), dtype=torch.uint8, device=cuda_device)
     Y2 = torch.empty_like(Y1)
     w8.linear_quant_stage(Xd, ws)
     w8.linear_gemm_stage(256, 1024, Wp, sw, bd, Y2, ws)
@@ -139,7 +139,7 @@ def test_linear_repeat_calls_reuse_workspace(cuda_device):
     dev = cuda_device
     Wq, sw = w8.quantize_weight(W.to(dev))
     Wp = w8.pack_weight(Wq)
-    ws = torch.empty(w8.workspace_bytes(300, 512), dtype=torch.uint8, device=dev)
+    ws = torch.empty(w8.workspace_bytes(300, 256, 512), dtype=torch.uint8, device=dev)
     Xd, bd = X.to(dev), b.to(dev)
     outs = [w8.linear(Xd, Wp, sw, bd, workspace=ws) for _ in range(3)]
     torch.cuda.synchronize()
@@ -163,3 +163,45 @@ def test_guard_rejects_without_launch(cuda_device):
     sw = torch.ones(16, device=cuda_device)
     with pytest.raises(w8.UnsupportedShape):
         w8.linear(X, Wp, sw)
+
+
+def test_linear_k_split_workspace_sizes_identical(cuda_device):
+    """The full-size video projection with the workspace that w8a8_linear
+    asks for (last wave cut along K), with a smaller one (fewer segments) and
+    with the smallest accepted (whole tiles only): identical bytes."""
+    dev = cuda_device
+    M, N, K = 6144, 4096, 4096
+    X, W, b = wl.make("video")
+    Xd, bd = X.to(dev), b.to(dev)
+    Wq, sw = w8.quantize_weight(W.to(dev))
+    Wp = w8.pack_weight(Wq)
+    slot = 128 * 256 * 4
+    outs = []
+    for size in (w8.workspace_bytes(M, N, K), w8.workspace_min_bytes(M, K) + 100 * slot,
+                 w8.workspace_min_bytes(M, K)):
+        ws = torch.empty(size, dtype=torch.uint8, device=dev)
+        outs.append(w8.linear(Xd, Wp, sw, bd, workspace=ws))
+        assert w8.read_status(ws) == (0, 0)
+    torch.cuda.synchronize()
+    assert w8.gemm_plan(M, N, K)[1] == 5
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_linear_pair_and_single_cta_forms_identical(cuda_device):
+    """The video projection through the CTA-pair GEMM and through the
+    single-CTA GEMM: identical bytes (both are the exact INT32 accumulator
+    followed by the same fp32 epilogue)."""
+    dev = cuda_device
+    X, W, b = wl.make("video")
+    Xd, bd = X.to(dev), b.to(dev)
+    Wq, sw = w8.quantize_weight(W.to(dev))
+    Wp = w8.pack_weight(Wq)
+    pair = w8.linear(Xd, Wp, sw, bd)
+    w8.debug_force_single_cta(True)
+    try:
+        single = w8.linear(Xd, Wp, sw, bd)
+    finally:
+        w8.debug_force_single_cta(False)
+    torch.cuda.synchronize()
+    assert torch.equal(pair.view(torch.int16), single.view(torch.int16))

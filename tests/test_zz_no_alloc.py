@@ -57,7 +57,7 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device):
 def test_noalloc_full_video_projection(cuda_device):
     """The bench's workload (M=6144, K=N=4096) fits the built-in array."""
     X, Wp, sw, b = _layer("video", 6144, 4096, 4096, cuda_device)
-    assert w8.workspace_bytes(6144, 4096) <= w8.NOALLOC_SCRATCH_BYTES
+    assert w8.workspace_min_bytes(6144, 4096) <= w8.NOALLOC_SCRATCH_BYTES
     y = w8.linear_noalloc(X, Wp, sw, b)
     ref = w8.linear(X, Wp, sw, b)
     torch.cuda.synchronize()
@@ -66,7 +66,7 @@ def test_noalloc_full_video_projection(cuda_device):
 
 def test_noalloc_refuses_oversized_shape(cuda_device):
     M, K = 8192, 4096                     # workspace 64 MiB + headers: one byte too many is enough
-    assert w8.workspace_bytes(M, K) > w8.NOALLOC_SCRATCH_BYTES
+    assert w8.workspace_min_bytes(M, K) > w8.NOALLOC_SCRATCH_BYTES
     X = torch.zeros((M, K), dtype=torch.bfloat16, device=cuda_device)
     Wp = torch.zeros((64, K), dtype=torch.bfloat16, device=cuda_device)
     sw = torch.ones(64, device=cuda_device)

@@ -19,8 +19,8 @@ import torch
 
 __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
-    "quantize_act", "pack_weight", "workspace_bytes", "linear", "linear_quant_stage",
-    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "read_status", "set_wait_limit_ns", "debug_skip_loads",
+    "quantize_act", "pack_weight", "workspace_bytes", "workspace_min_bytes", "gemm_plan", "linear", "linear_quant_stage",
+    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
     "W8A8Linear", "F32", "BF16", "MAX_K",
 ]
 
@@ -71,7 +71,9 @@ def _load():
         "w8a8_quantize_weight": ([p, i32, i64, i64, p, p, p], i32),
         "w8a8_quantize_act": ([p, i32, i64, i64, p, p, p], i32),
         "w8a8_pack_weight": ([p, i64, i64, p, p], i32),
-        "w8a8_linear_workspace_bytes": ([i64, i64], sz),
+        "w8a8_linear_workspace_min_bytes": ([i64, i64], sz),
+        "w8a8_linear_workspace_bytes": ([i64, i64, i64], sz),
+        "w8a8_gemm_plan": ([i64, i64, i64, i32, i64, ctypes.POINTER(ctypes.c_int64)], i32),
         "w8a8_linear": ([p, i32, i64, i64, p, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_linear_quant_stage": ([p, i32, i64, i64, p, sz, p], i32),
         "w8a8_linear_gemm_stage": ([i64, i64, p, p, i64, p, i32, p, p, sz, p], i32),
@@ -80,6 +82,7 @@ def _load():
         "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "w8a8_debug_skip_loads": ([i32], None),
+        "w8a8_debug_force_single_cta": ([i32], None),
         "w8a8_status_str": ([i32], ctypes.c_char_p),
         "w8a8_version": ([], i32),
     }
@@ -167,17 +170,33 @@ def pack_weight(Wq: torch.Tensor, stream=None) -> torch.Tensor:
     return Wp
 
 
-def workspace_bytes(M: int, K: int) -> int:
-    return int(_load().w8a8_linear_workspace_bytes(M, K))
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace for full speed: codes, scales and the GEMM's split partial tiles."""
+    return int(_load().w8a8_linear_workspace_bytes(M, N, K))
 
 
-def _workspace(M, K, device, ws):
-    need = workspace_bytes(M, K)
-    if need == 0:
-        raise UnsupportedShape(4, "workspace size")
+def workspace_min_bytes(M: int, K: int) -> int:
+    """Smallest workspace accepted (no K-split of the GEMM's last wave)."""
+    return int(_load().w8a8_linear_workspace_min_bytes(M, K))
+
+
+def gemm_plan(M: int, N: int, K: int, num_sms: int = 0, max_slots: int = -1):
+    """(whole tiles, K-segments per remaining tile, segment units, CTAs,
+    CTAs per tile) of the GEMM's tile schedule, from the library's planner.
+    num_sms > 0 plans for that many SMs; 0 for the current device."""
+    out = (ctypes.c_int64 * 5)()
+    if not _load().w8a8_gemm_plan(M, N, K, num_sms, max_slots, out):
+        raise ValueError("invalid sizes for a plan: %d x %d x %d" % (M, N, K))
+    return tuple(int(v) for v in out)
+
+
+def _workspace(M, N, K, device, ws):
     if ws is None:
+        need = workspace_bytes(M, N, K)
+        if need == 0:
+            raise UnsupportedShape(4, "workspace size")
         ws = torch.empty((need,), dtype=torch.uint8, device=device)
-    elif ws.numel() * ws.element_size() < need:
+    elif ws.numel() * ws.element_size() < workspace_min_bytes(M, K):
         raise W8A8Error(5, "workspace")
     return ws
 
@@ -193,7 +212,7 @@ def linear(X: torch.Tensor, Wp: torch.Tensor, sw: torch.Tensor, bias=None, out=N
         raise ValueError("K mismatch: X %s, Wp %s" % (tuple(X.shape), tuple(Wp.shape)))
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
-    ws = _workspace(M, K, X.device, workspace)
+    ws = _workspace(M, N, K, X.device, workspace)
     bdt = _dt(bias) if bias is not None else BF16
     _check(_load().w8a8_linear(_ptr(X), _dt(X), M, K, _ptr(Wp), _ptr(sw), N, _ptr(bias), bdt, _ptr(out),
                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "w8a8_linear")
@@ -227,7 +246,7 @@ def gemm_s32(Xq: torch.Tensor, Wp: torch.Tensor, out=None, workspace=None, strea
     N = Wp.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.int32, device=Xq.device)
-    ws = _workspace(M, K, Xq.device, workspace)
+    ws = _workspace(M, N, K, Xq.device, workspace)
     _check(_load().w8a8_gemm_s32(_ptr(Xq), _ptr(Wp), M, N, K, _ptr(out), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)), "w8a8_gemm_s32")
     return out
@@ -274,6 +293,11 @@ def debug_skip_loads(on: bool):
     _load().w8a8_debug_skip_loads(1 if on else 0)
 
 
+def debug_force_single_cta(on: bool):
+    """Test hook: run every GEMM in the single-CTA form (128-row tiles)."""
+    _load().w8a8_debug_force_single_cta(1 if on else 0)
+
+
 class W8A8Linear:
     """A linear layer with static INT8 weights: quantises W once, then
     ``layer(X)`` runs the guarded W8A8 path (activation quantisation, tensor-core
@@ -292,7 +316,7 @@ class W8A8Linear:
 
     def __call__(self, X: torch.Tensor, out=None) -> torch.Tensor:
         M, K = X.shape
-        need = workspace_bytes(M, K)
+        need = workspace_bytes(M, self.out_features, K)
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty((need,), dtype=torch.uint8, device=X.device)
         return linear(X, self.Wp, self.sw, self.bias, out=out, workspace=self._ws)

@@ -14,19 +14,44 @@
 //   Y = bf16_rne(((float)acc * sx[m]) * sw[n] + bias[n])
 // and store the tile (or store acc itself, for the INT32 test entry point).
 //
-// Kernel shape (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: A (128 x 64) and B (256 x 64) bf16 tiles, 128-byte
-//               swizzle, into a 4-stage shared-memory ring (48 KB per stage)
-//   warp 1      tensor-memory owner and MMA issuer (one thread): per stage
-//               4 x tcgen05.mma 128x256x16 into one of two 256-column fp32
-//               accumulators; commits free the stage / publish the chunk
-//   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows)
-//               and one 128-column half of the tile
-// Two accumulators let the MMA fill one chunk while the epilogue drains the
-// other.  Every mbarrier wait is bounded by a wall-clock limit; a wait that
-// runs out sets a bit in the status word and the CTA unwinds (waiting,
-// again with a limit, for its own copies and MMAs in flight) and frees its
-// tensor memory.
+// Two forms, one persistent CTA per SM either way (10 warps):
+//   kPair = 1  a CTA owns a 128 x 256 output tile; per 64-deep k-block it
+//              loads A 128 x 64 and B 256 x 64 (48 KB, 4-stage ring) and
+//              issues tcgen05.mma.cta_group::1 128x256x16.
+//   kPair = 2  a cluster of two CTAs owns a 256 x 256 tile; each CTA loads
+//              its 128 rows of A and 128 of the 256 rows of B (32 KB,
+//              6-stage ring), and the even CTA issues tcgen05.mma.cta_group::2
+//              256x256x16, which reads both CTAs' shared memory and leaves
+//              each CTA's 128 rows of the accumulator in its own tensor
+//              memory.  Per SM this moves 2/3 of the operand bytes of the
+//              single-CTA form for the same MMA work, which is what keeps
+//              the tensor pipe fed when every SM streams operands at once.
+// Roles: warp 0 TMA producer; warp 1 tensor-memory owner and (in the leader
+// CTA) the single MMA-issuing thread; warps 2-9 epilogue, warp w reading
+// TMEM lanes 32*(w%4)..+31 (its rows) and one 128-column half of the tile.
+// Two 256-column fp32 accumulators let the MMA fill one chunk while the
+// epilogue drains the other.  In a pair, both CTAs' copies complete on the
+// leader's "full" barrier, which the leader's producer alone arms with the
+// bytes of both (the barrier's transaction count may run below zero while
+// the peer's bytes land first); the leader's commits arrive on both CTAs'
+// barriers, and both CTAs' epilogues release the leader's accumulator.
+//
+// Work units.  The host plans the tiles as whole-tile units dealt round-robin
+// to the workers (CTAs, or CTA pairs), except that when the last wave would
+// leave most of them idle (tiles % workers at most half of the workers), its
+// tiles are cut along K into `splits` segments, one per worker.  A segment
+// writes its INT32 partial (each CTA its own 128 rows) to the workspace,
+// fences, and counts itself in on the arrival counter of its (tile, CTA
+// rank); the segment that arrives last adds the other partials to its own
+// (INT32 addition is exact and associative, so the sum is the exact
+// accumulator) and runs the epilogue, then resets the counter.  No CTA ever
+// waits for another CTA's segment.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
+// sets a bit in the status word and the CTA unwinds (waiting, again with a
+// limit, for its own copies and MMAs in flight) and frees its tensor memory.
+// A pair meets at a cluster barrier after set-up and before tear-down; every
+// path through the kernel reaches both.
 #pragma once
 
 #include <cstdint>
@@ -37,19 +62,29 @@
 
 namespace w8a8 {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kBK = 64;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int kStages = 4;
+constexpr int kBM = 128;   // output rows per CTA
+constexpr int kBN = 256;   // output columns per tile
+constexpr int kBK = 64;    // 64 bf16 = 128 bytes = one swizzle row
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kUmmaK = 16;
-constexpr uint32_t kAStageBytes = kBM * kBK * 2;
-constexpr uint32_t kBStageBytes = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;  // two fp32 accumulators
 constexpr int kMaxKbPerChunk = 16;       // 16 * 64 = 1024: 1024 * 127^2 < 2^24
-constexpr size_t kGemmSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256 /* barriers */;
+constexpr int kPartialInt4 = kBM * kBN / 4;  // one CTA's INT32 partial tile, in 16-byte vectors
+constexpr int kEpiBarrier = 1;               // named barrier of the epilogue warps
+
+template <int kPair>
+struct GemmCfg {
+    static constexpr int kTileRows = kBM * kPair;                     // output rows per tile
+    static constexpr int kBRows = kBN / kPair;                        // rows of B each CTA loads
+    static constexpr uint32_t kAStageBytes = kBM * kBK * 2;
+    static constexpr uint32_t kBStageBytes = kBRows * kBK * 2;
+    static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
+    static constexpr int kStages = kPair == 2 ? 6 : 4;
+    static constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256 /* barriers */;
+};
+static_assert(GemmCfg<1>::kSmemBytes <= 227 * 1024 && GemmCfg<2>::kSmemBytes <= 227 * 1024, "shared memory");
+static_assert((2 * GemmCfg<2>::kStages + 5) * 8 + 4 <= 256, "barrier area");
 
 // Status bits (same values as W8A8_DEV_* in the public header).
 constexpr uint32_t kDevTimeoutProducer = 0x1;
@@ -62,11 +97,16 @@ struct GemmParams {
     int32_t kb_per_chunk;      // k-blocks of 64 per exact fp32 chunk, 1..16
     int32_t group_m;           // tile rasterisation: m-tiles per group
     int32_t bias_mode;         // 0 none, 1 fp32, 2 bf16
+    int32_t dp_tiles;          // tiles [0, dp_tiles) are whole-tile units, round-robin over the CTAs
+    int32_t splits;            // K-segments per remaining tile (1: no split)
+    int32_t tail_units;        // (tiles - dp_tiles) * splits; unit u runs on worker u
     const float* sx;           // [M]
     const float* sw;           // [N]
     const void* bias;          // [N] or nullptr
     void* out;                 // bf16 Y [M][N] or int32 acc [M][N]
     uint32_t* status;          // device status word
+    uint32_t* tile_counters;   // [(tiles - dp_tiles) * kPair] arrivals per split (tile, CTA rank)
+    int4* partials;            // [tail_units * kPair][kPartialInt4] INT32 partial tiles
     uint64_t wait_limit_ns;
     int32_t skip_loads;        // test hook: producer issues no copies
 };
@@ -82,47 +122,85 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     nb = r / gsz;
 }
 
+// One unit of work: k-blocks [kb0, kb1) of one output tile.  slot < 0 for a
+// whole tile; otherwise the tile is split and slot is the unit's partial slot.
+struct Unit {
+    int tile, kb0, kb1, slot;
+};
+
+// The i-th unit of worker `w` of `W` (false once there are no more).
+__device__ __forceinline__ bool worker_unit(const GemmParams& p, int num_kb, int w, int W, int i, Unit& u)
+{
+    const int n_dp = w < p.dp_tiles ? (p.dp_tiles - w + W - 1) / W : 0;
+    if (i < n_dp) {
+        u.tile = w + i * W;
+        u.kb0 = 0;
+        u.kb1 = num_kb;
+        u.slot = -1;
+        return true;
+    }
+    if (i == n_dp && w < p.tail_units) {
+        const int seg = w % p.splits;
+        u.tile = p.dp_tiles + w / p.splits;
+        u.kb0 = static_cast<int>(static_cast<int64_t>(seg) * num_kb / p.splits);
+        u.kb1 = static_cast<int>(static_cast<int64_t>(seg + 1) * num_kb / p.splits);
+        u.slot = w;
+        return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void epi_barrier()
+{
+    asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(32 * kEpiWarps) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-template <bool kOutS32>
+template <bool kOutS32, int kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_w8a8_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                              const GemmParams p)
 {
+    using C = GemmCfg<kPair>;
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kAStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* full = bars;                    // [kStages] TMA -> MMA
-    uint64_t* empty = bars + kStages;         // [kStages] MMA -> TMA
-    uint64_t* tfull = bars + 2 * kStages;     // [2] MMA -> epilogue
-    uint64_t* tempty = tfull + 2;             // [2] epilogue -> MMA
+    uint8_t* sB = smem + S * C::kAStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+    uint64_t* full = bars;                    // [S] TMA -> MMA (the leader's counts both CTAs' bytes)
+    uint64_t* empty = bars + S;               // [S] MMA -> TMA
+    uint64_t* tfull = bars + 2 * S;           // [2] MMA -> epilogue
+    uint64_t* tempty = tfull + 2;             // [2] epilogue -> MMA (the leader's counts both CTAs)
     uint64_t* done = tempty + 2;              // MMA teardown
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+    __shared__ int s_last_arrival;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tiles_m = (p.M + kBM - 1) / kBM;
+    const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
+    const int worker = kPair == 2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int workers = kPair == 2 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+    const int tiles_m = (p.M + C::kTileRows - 1) / C::kTileRows;
     const int tiles_n = (p.N + kBN - 1) / kBN;
-    const int num_tiles = tiles_m * tiles_n;
     const int num_kb = (p.K + kBK - 1) / kBK;
-    const int chunks = (num_kb + p.kb_per_chunk - 1) / p.kb_per_chunk;
     const uint64_t limit = p.wait_limit_ns;
+    constexpr uint16_t kBoth = kPair == 2 ? 0x3 : 0x1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], kEpiWarps);
+            mbar_init(&tempty[b], kPair * kEpiWarps);
         }
         mbar_init(done, 1);
         mbar_fence_init();
@@ -132,11 +210,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_desc(&tmap_b);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<kPair>(tmem_holder, kTmemCols);
+        tmem_relinquish<kPair>();
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kPair == 2) cluster_sync_all();   // both CTAs' barriers exist before any remote use
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -146,38 +225,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t it = 0;
             uint32_t issued_mask = 0, issued_par = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            Unit u;
+            for (int ui = 0; ok && worker_unit(p, num_kb, worker, workers, ui, u); ++ui) {
                 int mb, nb;
-                tile_coords(t, tiles_m, tiles_n, p.group_m, mb, nb);
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
-                    const int s = static_cast<int>(it % kStages);
-                    const uint32_t ph = (it / kStages) & 1u;
+                tile_coords(u.tile, tiles_m, tiles_n, p.group_m, mb, nb);
+                const int a_row = (mb * kPair + static_cast<int>(rank)) * kBM;
+                const int b_row = nb * kBN + static_cast<int>(rank) * C::kBRows;
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S);
+                    const uint32_t ph = (it / S) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, limit)) {
                         atomicOr(p.status, kDevTimeoutProducer);
                         ok = false;
                         break;
                     }
                     if (p.skip_loads) continue;
-                    mbar_arrive_expect_tx(&full[s], kStageBytes);
-                    tma_load_2d(sA + s * kAStageBytes, &tmap_a, &full[s], kb * kBK, mb * kBM);
-                    tma_load_2d(sB + s * kBStageBytes, &tmap_b, &full[s], kb * kBK, nb * kBN);
+                    if constexpr (kPair == 2) {
+                        const uint32_t bar = cluster_map(&full[s], 0);
+                        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+                        tma_load_2d_pair(sA + s * C::kAStageBytes, &tmap_a, bar, kb * kBK, a_row);
+                        tma_load_2d_pair(sB + s * C::kBStageBytes, &tmap_b, bar, kb * kBK, b_row);
+                    } else {
+                        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                        tma_load_2d(sA + s * C::kAStageBytes, &tmap_a, &full[s], kb * kBK, a_row);
+                        tma_load_2d(sB + s * C::kBStageBytes, &tmap_b, &full[s], kb * kBK, b_row);
+                    }
                     issued_mask |= 1u << s;
                     issued_par = (issued_par & ~(1u << s)) | (ph << s);
                 }
             }
-            // Copies still in flight must land before the CTA exits.
-            for (int s = 0; s < kStages; ++s)
-                if ((issued_mask >> s) & 1u)
-                    if (!mbar_wait(&full[s], (issued_par >> s) & 1u, limit)) atomicOr(p.status, kDevTimeoutTeardown);
+            // Copies still in flight must land before the CTA exits.  The
+            // leader's "full" barriers count both CTAs' copies; the peer
+            // CTA stays until the closing cluster barrier, which the leader
+            // reaches only after these waits.
+            if (rank == 0)
+                for (int s = 0; s < S; ++s)
+                    if ((issued_mask >> s) & 1u)
+                        if (!mbar_wait(&full[s], (issued_par >> s) & 1u, limit))
+                            atomicOr(p.status, kDevTimeoutTeardown);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+        // ------------------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(C::kTileRows, kBN);
             uint32_t it = 0, cc = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                for (int c = 0; c < chunks && ok; ++c, ++cc) {
+            Unit u;
+            for (int ui = 0; ok && worker_unit(p, num_kb, worker, workers, ui, u); ++ui) {
+                for (int kc0 = u.kb0; kc0 < u.kb1 && ok; kc0 += p.kb_per_chunk, ++cc) {
                     const uint32_t b = cc & 1u;
                     const uint32_t bph = (cc >> 1) & 1u;
                     if (!mbar_wait(&tempty[b], bph ^ 1u, limit)) {
@@ -187,46 +282,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + b * kBN;
-                    const int kb0 = c * p.kb_per_chunk;
-                    const int kb1 = min(num_kb, kb0 + p.kb_per_chunk);
-                    for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                        const int s = static_cast<int>(it % kStages);
-                        const uint32_t ph = (it / kStages) & 1u;
+                    const int kc1 = min(u.kb1, kc0 + p.kb_per_chunk);
+                    for (int kb = kc0; kb < kc1; ++kb, ++it) {
+                        const int s = static_cast<int>(it % S);
+                        const uint32_t ph = (it / S) & 1u;
                         if (!mbar_wait(&full[s], ph, limit)) {
                             atomicOr(p.status, kDevTimeoutMma);
                             ok = false;
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint32_t a0 = smem_addr(sA + s * kAStageBytes);
-                        const uint32_t b0 = smem_addr(sB + s * kBStageBytes);
+                        const uint32_t a0 = smem_addr(sA + s * C::kAStageBytes);
+                        const uint32_t b0 = smem_addr(sB + s * C::kBStageBytes);
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            mma_bf16(d_tmem, smem_desc_k128(a0 + k * kUmmaK * 2), smem_desc_k128(b0 + k * kUmmaK * 2),
-                                     idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                            mma_bf16<kPair>(d_tmem, smem_desc_k128(a0 + k * kUmmaK * 2),
+                                            smem_desc_k128(b0 + k * kUmmaK * 2), idesc,
+                                            (kb > kc0 || k > 0) ? 1u : 0u);
                         }
-                        mma_commit(&empty[s]);
+                        mma_commit<kPair>(&empty[s], kBoth);
                     }
-                    if (ok) mma_commit(&tfull[b]);
+                    if (ok) mma_commit<kPair>(&tfull[b], kBoth);
                 }
             }
             // Every MMA issued must complete before tensor memory is freed.
-            mma_commit(done);
+            mma_commit<kPair>(done, 0x1);
             if (!mbar_wait(done, 0, limit)) atomicOr(p.status, kDevTimeoutTeardown);
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;        // TMEM lanes this warp may read
         const int half = (warp - 2) >> 2;    // which 128 columns of the tile
+        const int e = warp - 2;              // epilogue warp index, 0..7
         uint32_t cc = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        Unit u;
+        for (int ui = 0; ok && worker_unit(p, num_kb, worker, workers, ui, u); ++ui) {
             int mb, nb;
-            tile_coords(t, tiles_m, tiles_n, p.group_m, mb, nb);
+            tile_coords(u.tile, tiles_m, tiles_n, p.group_m, mb, nb);
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
-            for (int c = 0; c < chunks; ++c, ++cc) {
+            for (int kc0 = u.kb0; kc0 < u.kb1; kc0 += p.kb_per_chunk, ++cc) {
                 const uint32_t b = cc & 1u;
                 const uint32_t bph = (cc >> 1) & 1u;
                 int got = 1;
@@ -250,11 +347,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[b]);
+                if (lane == 0) {
+                    if constexpr (kPair == 2)
+                        mbar_arrive_cluster(cluster_map(&tempty[b], 0));
+                    else
+                        mbar_arrive(&tempty[b]);
+                }
             }
             if (!ok) break;
 
-            const int m = mb * kBM + quarter * 32 + lane;
+            if (u.slot >= 0) {
+                // A K-segment of a split tile: publish this CTA's partial sums,
+                // count in, and only the last segment to arrive finishes this
+                // CTA's rows of the tile.  Thread (e, lane) always holds the
+                // same 128 sums, so the slots use a layout in which each warp
+                // access is 512 contiguous bytes.
+                int4* mine = p.partials + (static_cast<int64_t>(u.slot) * kPair + rank) * kPartialInt4;
+#pragma unroll
+                for (int g = 0; g < 32; ++g)
+                    __stcg(mine + (e * 32 + g) * 32 + lane,
+                           make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
+                __threadfence();
+                epi_barrier();
+                const int counter = (u.tile - p.dp_tiles) * kPair + static_cast<int>(rank);
+                if (e == 0 && lane == 0)
+                    s_last_arrival =
+                        (atomicAdd(p.tile_counters + counter, 1u) == static_cast<uint32_t>(p.splits - 1)) ? 1 : 0;
+                epi_barrier();
+                if (!s_last_arrival) continue;
+                __threadfence();
+                const int first = (u.tile - p.dp_tiles) * p.splits;
+                for (int unit = first; unit < first + p.splits; ++unit) {
+                    if (unit == u.slot) continue;
+                    const int4* other = p.partials + (static_cast<int64_t>(unit) * kPair + rank) * kPartialInt4 +
+                                        e * 32 * 32 + lane;
+                    // Eight 16-byte loads in flight per batch: enough to cover
+                    // L2 latency across 256 threads, few enough registers that
+                    // the 128 running sums stay in registers.
+#pragma unroll
+                    for (int gb = 0; gb < 32; gb += 8) {
+                        int4 v[8];
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) v[g] = __ldcg(other + (gb + g) * 32);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            acc[4 * (gb + g)] += v[g].x;
+                            acc[4 * (gb + g) + 1] += v[g].y;
+                            acc[4 * (gb + g) + 2] += v[g].z;
+                            acc[4 * (gb + g) + 3] += v[g].w;
+                        }
+                        asm volatile("" ::: "memory");   // keep the batches apart
+                    }
+                }
+                if (e == 0 && lane == 0) p.tile_counters[counter] = 0u;   // ready for the next launch
+            }
+
+            const int m = (mb * kPair + static_cast<int>(rank)) * kBM + quarter * 32 + lane;
             const int n0 = nb * kBN + half * 128;
             if (m < p.M) {
                 if constexpr (kOutS32) {
@@ -310,8 +458,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    // A pair leaves together: the leader's MMAs are complete (it waited on
+    // `done`) and its copies have landed before either CTA frees tensor
+    // memory or exits while the other may still target its shared memory.
+    if constexpr (kPair == 2) cluster_sync_all();
     tc_fence_after_sync();
-    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 1) tmem_dealloc<kPair>(tmem_base, kTmemCols);
 }
 
 }  // namespace w8a8

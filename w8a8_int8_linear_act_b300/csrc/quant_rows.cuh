@@ -37,6 +37,7 @@ namespace w8a8 {
 constexpr float kRoundMagic = 12582912.0f;            // 1.5 * 2^23
 constexpr uint32_t kRoundMagicBits = 0x4B400000u;
 constexpr float kNearHalf = 0.5f - 0.00006103515625f; // 0.5 - 2^-14
+constexpr int kHeaderWords = 256;                     // workspace header: 1 KB of 32-bit words
 
 template <typename TIn>
 struct InVec;
@@ -196,7 +197,8 @@ __device__ __forceinline__ void quantize_vector(const uint4& v, const RowScale& 
 
 // NV > 0: each thread keeps up to NV vectors of the row in registers (single
 // HBM read).  NV == 0: two passes over the row (for very long rows).
-// `status`, when not NULL, is cleared by block 0 (start of a linear call).
+// `status`, when not NULL, is the workspace header (status word and the
+// GEMM's split-tile counters), cleared by block 0 at the start of a call.
 template <typename TIn, bool kBf16Codes, int NV>
 __global__ void __launch_bounds__(1024) quant_rows_kernel(const TIn* __restrict__ A, int64_t K,
                                                           void* __restrict__ Q, float* __restrict__ S,
@@ -212,7 +214,8 @@ __global__ void __launch_bounds__(1024) quant_rows_kernel(const TIn* __restrict_
     const int64_t out0 = row * K;
     const int T = blockDim.x;
 
-    if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    if (status != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) status[i] = 0u;
 
     uint32_t m2 = 0;
     if constexpr (NV > 0) {
@@ -241,11 +244,12 @@ __global__ void __launch_bounds__(1024) quant_rows_kernel(const TIn* __restrict_
 }
 
 // int8 codes -> the same integers as bf16 (exact), 16 codes per thread step.
-// `status`, when not NULL, is cleared by thread 0 of block 0.
+// `status`, when not NULL, is the workspace header, cleared by block 0.
 __global__ void codes_to_bf16_kernel(const int8_t* __restrict__ Qi, uint16_t* __restrict__ Qb, int64_t n16,
                                      uint32_t* __restrict__ status)
 {
-    if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    if (status != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) status[i] = 0u;
     const uint4* src = reinterpret_cast<const uint4*>(Qi);
     uint4* dst = reinterpret_cast<uint4*>(Qb);
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;

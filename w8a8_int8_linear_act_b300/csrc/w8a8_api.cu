@@ -22,12 +22,14 @@ constexpr int kMaxDevices = 64;
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_skip_loads{0};
+std::atomic<int> g_force_single{0};
 
 struct DeviceInfo {
     bool ready = false;
     bool supported = false;
     int num_sms = 0;
     bool gemm_attr_set = false;
+    int pair_workers = 0;   // co-resident CTA pairs of the 2-CTA GEMM (0: form unavailable)
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -95,9 +97,19 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t in
 
 // Workspace layout, relative to the first 1024-byte boundary at or after the
 // caller's pointer (the caller only guarantees 16 bytes; kAlign bytes of
-// slack are part of the size): status word, row scales, activation codes.
+// slack are part of the size):
+//   header  1 KB: status word (word 0), split-tile arrival counters (words
+//           16 ..), cleared by the first kernel of every call
+//   sx      M fp32 row scales
+//   codes   M x K activation codes as bf16
+//   slots   INT32 partial tiles of the GEMM's K-split last wave, as many as
+//           fit in what the caller gave (none is fine: no split then)
+constexpr size_t kCounterOffWords = 16;
+constexpr int kMaxSplitTiles = 256 - static_cast<int>(kCounterOffWords);   // counters: split tiles x CTAs per tile
+constexpr size_t kSlotBytes = static_cast<size_t>(w8a8::kPartialInt4) * 16u;
+
 struct WsLayout {
-    size_t status_off, sx_off, codes_off, total;
+    size_t status_off, sx_off, codes_off, slots_off, min_total;
 };
 
 bool ws_layout(int64_t M, int64_t K, WsLayout* L)
@@ -106,13 +118,126 @@ bool ws_layout(int64_t M, int64_t K, WsLayout* L)
     L->status_off = 0;
     L->sx_off = kAlign;
     L->codes_off = L->sx_off + align_up(static_cast<size_t>(M) * 4u, kAlign);
-    L->total = kAlign + L->codes_off + align_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2u, kAlign);
+    L->slots_off = L->codes_off + align_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2u, kAlign);
+    L->min_total = kAlign + L->slots_off;
     return true;
+}
+
+// Partial-tile slots that fit in a workspace of ws_bytes.
+int64_t ws_slots(const WsLayout& L, size_t ws_bytes)
+{
+    return ws_bytes > L.min_total ? static_cast<int64_t>((ws_bytes - L.min_total) / kSlotBytes) : 0;
 }
 
 uint8_t* ws_base(const void* ws)
 {
     return reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(ws), kAlign));
+}
+
+// How the GEMM deals its output tiles to its workers (see gemm_tcgen05.cuh).
+// A worker is one CTA (128-row tiles) or, for M > 128, a CTA pair on two
+// SMs (256-row tiles).  Full waves run whole tiles.  When the last wave
+// would be at most half full, its `rem` tiles are cut along K into `splits`
+// segments so that all workers share that wave.  The last segment of a tile
+// to finish adds the other partials (each one 128 x 256 INT32 block read
+// from L2), so more segments cost more fix-up: splits stays near
+// sqrt(k-blocks), which balances the segment's MMA time (k-blocks / splits)
+// against that fix-up ((splits - 1) reads).
+struct GemmPlan {
+    int pair;          // CTAs per tile: 1 or 2
+    int64_t dp_tiles;
+    int splits;
+    int64_t tail_units;
+    int grid;          // CTAs launched
+};
+
+constexpr int kMinKbPerSplit = 2;
+
+// `workers`: CTAs (pair 1) or co-resident CTA pairs (pair 2).
+// `max_slots`: partial-tile slots (128 x 256 INT32 each) in the workspace.
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int pair, int workers, int64_t max_slots)
+{
+    const int64_t tile_rows = static_cast<int64_t>(w8a8::kBM) * pair;
+    const int64_t tiles = ((M + tile_rows - 1) / tile_rows) * ((N + w8a8::kBN - 1) / w8a8::kBN);
+    const int64_t num_kb = (K + w8a8::kBK - 1) / w8a8::kBK;
+    GemmPlan g;
+    g.pair = pair;
+    g.dp_tiles = tiles;
+    g.splits = 1;
+    g.tail_units = 0;
+    g.grid = static_cast<int>(tiles < workers ? tiles : workers) * pair;
+    const int64_t rem = tiles % workers;
+    if (rem == 0 || 2 * rem > workers || rem * pair > kMaxSplitTiles) return g;
+    int64_t s = workers / rem;
+    int64_t root = 1;
+    while ((root + 1) * (root + 1) <= num_kb) ++root;
+    if (s > root) s = root;
+    if (s > num_kb / kMinKbPerSplit) s = num_kb / kMinKbPerSplit;
+    if (s > max_slots / pair / rem) s = max_slots / pair / rem;
+    if (s < 2) return g;
+    g.dp_tiles = tiles - rem;
+    g.splits = static_cast<int>(s);
+    g.tail_units = rem * s;
+    g.grid = static_cast<int>(tiles >= workers ? workers : g.tail_units) * pair;
+    return g;
+}
+
+// The 2-CTA form for M > 128 when the device can hold CTA pairs (and the
+// single-CTA test switch is off); the single-CTA form otherwise.
+GemmPlan choose_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_workers, int64_t max_slots)
+{
+    if (M > w8a8::kBM && pair_workers >= 1 && !g_force_single.load())
+        return plan_gemm(M, N, K, 2, pair_workers, max_slots);
+    return plan_gemm(M, N, K, 1, num_sms, max_slots);
+}
+
+template <bool kOutS32, int kPair>
+cudaError_t set_gemm_smem()
+{
+    return cudaFuncSetAttribute(w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, kPair>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(w8a8::GemmCfg<kPair>::kSmemBytes));
+}
+
+// Shared-memory attributes of the four GEMM instantiations, and how many CTA
+// pairs the 2-CTA form can hold at once on this device; once per device.
+bool ensure_gemm_ready(DeviceInfo* dev)
+{
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (dev->gemm_attr_set) return true;
+    if (set_gemm_smem<false, 1>() != cudaSuccess || set_gemm_smem<true, 1>() != cudaSuccess ||
+        set_gemm_smem<false, 2>() != cudaSuccess || set_gemm_smem<true, 2>() != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(dev->num_sms / 2 > 0 ? dev->num_sms / 2 : 1));
+    cfg.blockDim = dim3(w8a8::kGemmThreads);
+    cfg.dynamicSmemBytes = w8a8::GemmCfg<2>::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, w8a8::gemm_w8a8_tcgen05_kernel<false, 2>, &cfg) != cudaSuccess)
+        clusters = 0;
+    cudaGetLastError();
+    dev->pair_workers = clusters > dev->num_sms / 2 ? dev->num_sms / 2 : clusters;
+    dev->gemm_attr_set = true;
+    return true;
+}
+
+// Plan for the current device (a 148-SM device with 74 pairs when none is
+// current), as the launch will make it.
+GemmPlan current_plan(int64_t M, int64_t N, int64_t K, int64_t max_slots)
+{
+    int dno = 0;
+    DeviceInfo* d = const_cast<DeviceInfo*>(device_info(&dno));
+    if (d && ensure_gemm_ready(d)) return choose_plan(M, N, K, d->num_sms, d->pair_workers, max_slots);
+    return choose_plan(M, N, K, 148, 74, max_slots);
 }
 
 int guard_reasons(int64_t M, int64_t N, int64_t K, int x_dtype, int bias_dtype)
@@ -207,27 +332,13 @@ w8a8_status launch_codes_to_bf16(const int8_t* Qi, uint16_t* Qb, int64_t n, uint
 template <bool kOutS32>
 w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t* Wp, int64_t M, int64_t N,
                         int64_t K, const float* sx, const float* sw, const void* bias, int bias_mode, void* out,
-                        uint32_t* status, cudaStream_t stream)
+                        uint8_t* ws_aligned, const WsLayout& L, int64_t slots, cudaStream_t stream)
 {
+    if (!ensure_gemm_ready(dev)) return W8A8_ERR_CUDA;
+    const GemmPlan g = choose_plan(M, N, K, dev->num_sms, dev->pair_workers, slots);
     CUtensorMap ta, tb;
     if (!encode_bf16_2d(&ta, A_codes, M, K, w8a8::kBM)) return W8A8_ERR_CUDA;
-    if (!encode_bf16_2d(&tb, Wp, N, K, w8a8::kBN)) return W8A8_ERR_CUDA;
-    auto kern = w8a8::gemm_w8a8_tcgen05_kernel<kOutS32>;
-    {
-        std::lock_guard<std::mutex> lock(g_dev_mutex);
-        if (!dev->gemm_attr_set) {
-            if (cudaFuncSetAttribute(w8a8::gemm_w8a8_tcgen05_kernel<false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(w8a8::kGemmSmemBytes)) != cudaSuccess ||
-                cudaFuncSetAttribute(w8a8::gemm_w8a8_tcgen05_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(w8a8::kGemmSmemBytes)) != cudaSuccess) {
-                cudaGetLastError();
-                return W8A8_ERR_CUDA;
-            }
-            dev->gemm_attr_set = true;
-        }
-    }
+    if (!encode_bf16_2d(&tb, Wp, N, K, static_cast<uint32_t>(w8a8::kBN / g.pair))) return W8A8_ERR_CUDA;
     w8a8::GemmParams p;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
@@ -239,12 +350,36 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     p.sw = sw;
     p.bias = bias;
     p.out = out;
-    p.status = status;
+    uint32_t* header = reinterpret_cast<uint32_t*>(ws_aligned + L.status_off);
+    p.status = header;
+    p.tile_counters = header + kCounterOffWords;
+    p.partials = reinterpret_cast<int4*>(ws_aligned + L.slots_off);
     p.wait_limit_ns = g_wait_limit_ns.load();
     p.skip_loads = g_skip_loads.load();
-    const int64_t tiles = ((M + w8a8::kBM - 1) / w8a8::kBM) * ((N + w8a8::kBN - 1) / w8a8::kBN);
-    const int grid = static_cast<int>(tiles < dev->num_sms ? tiles : dev->num_sms);
-    kern<<<grid, w8a8::kGemmThreads, w8a8::kGemmSmemBytes, stream>>>(ta, tb, p);
+    p.dp_tiles = static_cast<int32_t>(g.dp_tiles);
+    p.splits = g.splits;
+    p.tail_units = static_cast<int32_t>(g.tail_units);
+    if (g.pair == 1) {
+        w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 1>
+            <<<g.grid, w8a8::kGemmThreads, w8a8::GemmCfg<1>::kSmemBytes, stream>>>(ta, tb, p);
+        return last_launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(g.grid));
+    cfg.blockDim = dim3(w8a8::kGemmThreads);
+    cfg.dynamicSmemBytes = w8a8::GemmCfg<2>::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 2>, ta, tb, p) != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
     return last_launch_status();
 }
 
@@ -312,11 +447,34 @@ w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, uint16_t* W
     return launch_codes_to_bf16(Wq, Wp, N * K, nullptr, dev->num_sms, static_cast<cudaStream_t>(stream));
 }
 
-size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K)
+size_t w8a8_linear_workspace_min_bytes(int64_t M, int64_t K)
 {
     WsLayout L;
-    return ws_layout(M, K, &L) ? L.total : 0;
+    return ws_layout(M, K, &L) ? L.min_total : 0;
 }
+
+size_t w8a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    WsLayout L;
+    if (N < 1 || N > INT32_MAX || !ws_layout(M, K, &L)) return 0;
+    const GemmPlan g = current_plan(M, N, K, INT64_MAX);
+    return L.min_total + static_cast<size_t>(g.tail_units * g.pair) * kSlotBytes;
+}
+
+int w8a8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t max_slots, int64_t* plan)
+{
+    if (!plan || M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return 0;
+    const int64_t slots = max_slots < 0 ? INT64_MAX : max_slots;
+    const GemmPlan g = num_sms > 0 ? choose_plan(M, N, K, num_sms, num_sms / 2, slots) : current_plan(M, N, K, slots);
+    plan[0] = g.dp_tiles;
+    plan[1] = g.splits;
+    plan[2] = g.tail_units;
+    plan[3] = g.grid;
+    plan[4] = g.pair;
+    return 1;
+}
+
+void w8a8_debug_force_single_cta(int on) { g_force_single.store(on ? 1 : 0); }
 
 w8a8_status w8a8_linear_quant_stage(const void* X, int x_dtype, int64_t M, int64_t K, void* ws, size_t ws_bytes,
                                     void* stream)
@@ -325,7 +483,7 @@ w8a8_status w8a8_linear_quant_stage(const void* X, int x_dtype, int64_t M, int64
     if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
     if (M < 1 || M > INT32_MAX || K < 16 || K % 16 != 0 || K > W8A8_MAX_K) return W8A8_ERR_UNSUPPORTED_SHAPE;
     WsLayout L;
-    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
     if (!aligned(X, 16) || !aligned(ws, 16)) return W8A8_ERR_ALIGNMENT;
     if (!device_info(nullptr)) return W8A8_ERR_NO_DEVICE;
     uint8_t* w = ws_base(ws);
@@ -341,7 +499,7 @@ w8a8_status w8a8_linear_gemm_stage(int64_t M, int64_t K, const uint16_t* Wp, con
     if (bias && bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
     if (guard_reasons(M, N, K, W8A8_BF16, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
     WsLayout L;
-    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
     if (!aligned(Wp, 16) || !aligned(Y, 16) || !aligned(ws, 16) || !aligned(sw, 16)) return W8A8_ERR_ALIGNMENT;
     if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
     int devno = 0;
@@ -350,8 +508,8 @@ w8a8_status w8a8_linear_gemm_stage(int64_t M, int64_t K, const uint16_t* Wp, con
     uint8_t* w = ws_base(ws);
     const int bias_mode = bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0;
     return launch_gemm<false>(dev, reinterpret_cast<const uint16_t*>(w + L.codes_off), Wp, M, N, K,
-                              reinterpret_cast<const float*>(w + L.sx_off), sw, bias, bias_mode, Y,
-                              reinterpret_cast<uint32_t*>(w + L.status_off), static_cast<cudaStream_t>(stream));
+                              reinterpret_cast<const float*>(w + L.sx_off), sw, bias, bias_mode, Y, w, L,
+                              ws_slots(L, ws_bytes), static_cast<cudaStream_t>(stream));
 }
 
 w8a8_status w8a8_linear(const void* X, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp, const float* sw,
@@ -364,7 +522,7 @@ w8a8_status w8a8_linear(const void* X, int x_dtype, int64_t M, int64_t K, const 
     if (bias && bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
     if (guard_reasons(M, N, K, x_dtype, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
     WsLayout L;
-    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
     if (!aligned(X, 16) || !aligned(Wp, 16) || !aligned(Y, 16) || !aligned(ws, 16) || !aligned(sw, 16))
         return W8A8_ERR_ALIGNMENT;
     if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
@@ -379,7 +537,7 @@ w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64
     if (!Xq || !Wp || !acc || M < 0 || N < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
     if (guard_reasons(M, N, K, W8A8_BF16, W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
     WsLayout L;
-    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.total) return W8A8_ERR_WORKSPACE;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
     if (!aligned(Xq, 16) || !aligned(Wp, 16) || !aligned(acc, 16) || !aligned(ws, 16))
         return W8A8_ERR_ALIGNMENT;
     int devno = 0;
@@ -391,7 +549,8 @@ w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64
     uint16_t* codes = reinterpret_cast<uint16_t*>(w + L.codes_off);
     w8a8_status st = launch_codes_to_bf16(Xq, codes, M * K, status, dev->num_sms, s);
     if (st != W8A8_OK) return st;
-    return launch_gemm<true>(dev, codes, Wp, M, N, K, nullptr, nullptr, nullptr, 0, acc, status, s);
+    return launch_gemm<true>(dev, codes, Wp, M, N, K, nullptr, nullptr, nullptr, 0, acc, w, L, ws_slots(L, ws_bytes),
+                             s);
 }
 
 w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp,
@@ -400,7 +559,7 @@ w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K
 {
     WsLayout L;
     if (M < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
-    if (ws_layout(M, K, &L) && L.total > W8A8_NOALLOC_SCRATCH_BYTES) return W8A8_ERR_WORKSPACE;
+    if (ws_layout(M, K, &L) && L.min_total > W8A8_NOALLOC_SCRATCH_BYTES) return W8A8_ERR_WORKSPACE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
