@@ -80,11 +80,18 @@ struct GemmCfg {
     static constexpr uint32_t kAStageBytes = kBM * kBK * 2;
     static constexpr uint32_t kBStageBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
-    static constexpr int kStages = kPair == 2 ? 6 : 4;
-    static constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256 /* barriers */;
+    static constexpr int kStages = 4;
+    // Pair form: the bf16 output tile is staged in shared memory (per
+    // epilogue warp two 32-row x 64-column boxes, 128-byte swizzled) and
+    // written by TMA stores.
+    static constexpr uint32_t kStagingBytes = kPair == 2 ? kEpiWarps * 2 * 4096 : 0;
+    static constexpr uint32_t kParamBytes = 2 * kBN * 4;            // the tile's sw and bias, fp32
+    static constexpr size_t kSmemBytes =
+        1024 /* alignment slack */ + kStages * kStageBytes + kStagingBytes + kParamBytes + 256 /* barriers */;
 };
 static_assert(GemmCfg<1>::kSmemBytes <= 227 * 1024 && GemmCfg<2>::kSmemBytes <= 227 * 1024, "shared memory");
-static_assert((2 * GemmCfg<2>::kStages + 5) * 8 + 4 <= 256, "barrier area");
+static_assert((2 * GemmCfg<2>::kStages + 5) * 8 + 4 <= 256 && (2 * GemmCfg<1>::kStages + 5) * 8 + 4 <= 256,
+              "barrier area");
 
 // Status bits (same values as W8A8_DEV_* in the public header).
 constexpr uint32_t kDevTimeoutProducer = 0x1;
@@ -164,7 +171,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 template <bool kOutS32, int kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_w8a8_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                             const GemmParams p)
+                             const __grid_constant__ CUtensorMap tmap_y, const GemmParams p)
 {
     using C = GemmCfg<kPair>;
     constexpr int S = C::kStages;
@@ -173,7 +180,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * C::kAStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+    uint8_t* sOut = smem + S * C::kStageBytes;                      // pair form: output staging
+    float* s_sw = reinterpret_cast<float*>(sOut + C::kStagingBytes);  // [kBN] this tile's sw
+    float* s_bias = s_sw + kBN;                                      // [kBN] this tile's bias
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_bias + kBN);
     uint64_t* full = bars;                    // [S] TMA -> MMA (the leader's counts both CTAs' bytes)
     uint64_t* empty = bars + S;               // [S] MMA -> TMA
     uint64_t* tfull = bars + 2 * S;           // [2] MMA -> epilogue
@@ -181,6 +191,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* done = tempty + 2;              // MMA teardown
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
     __shared__ int s_last_arrival;
+    __shared__ int s_chunk_ready[2];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -208,6 +219,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
+        if constexpr (kPair == 2 && !kOutS32) tma_prefetch_desc(&tmap_y);
     }
     if (warp == 1) {
         tmem_alloc<kPair>(tmem_holder, kTmemCols);
@@ -320,17 +332,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int ui = 0; ok && worker_unit(p, num_kb, worker, workers, ui, u); ++ui) {
             int mb, nb;
             tile_coords(u.tile, tiles_m, tiles_n, p.group_m, mb, nb);
+            const int m = (mb * kPair + static_cast<int>(rank)) * kBM + quarter * 32 + lane;
+            const int n0 = nb * kBN + half * 128;
+            // The tile's column parameters, one column per epilogue thread,
+            // fetched now so that their latency hides behind the K loop.
+            epi_barrier();   // the previous unit's epilogue is done reading them
+            float sxm = 0.0f;
+            if constexpr (!kOutS32) {
+                const int i = e * 32 + lane;
+                const int n = nb * kBN + i;
+                s_sw[i] = n < p.N ? p.sw[n] : 0.0f;
+                if (p.bias_mode == 1)
+                    s_bias[i] = n < p.N ? static_cast<const float*>(p.bias)[n] : 0.0f;
+                else if (p.bias_mode == 2)
+                    s_bias[i] = n < p.N ? __uint_as_float(static_cast<uint32_t>(
+                                              static_cast<const uint16_t*>(p.bias)[n]) << 16)
+                                        : 0.0f;
+                if (m < p.M) sxm = p.sx[m];
+            }
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
             for (int kc0 = u.kb0; kc0 < u.kb1; kc0 += p.kb_per_chunk, ++cc) {
                 const uint32_t b = cc & 1u;
                 const uint32_t bph = (cc >> 1) & 1u;
-                int got = 1;
-                if (lane == 0) got = mbar_wait(&tfull[b], bph, limit) ? 1 : 0;
-                got = __shfl_sync(0xFFFFFFFFu, got, 0);
-                if (!got) {
-                    if (lane == 0) atomicOr(p.status, kDevTimeoutEpilogue);
+                // One thread takes the bounded wait for the whole epilogue and
+                // publishes the outcome, so all eight warps take the same path
+                // (their named barriers below could never complete otherwise).
+                if (e == 0 && lane == 0) s_chunk_ready[cc & 1u] = mbar_wait(&tfull[b], bph, limit) ? 1 : 0;
+                epi_barrier();
+                if (!s_chunk_ready[cc & 1u]) {
+                    if (e == 0 && lane == 0) atomicOr(p.status, kDevTimeoutEpilogue);
                     ok = false;
                     break;
                 }
@@ -402,10 +434,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (e == 0 && lane == 0) p.tile_counters[counter] = 0u;   // ready for the next launch
             }
 
-            const int m = (mb * kPair + static_cast<int>(rank)) * kBM + quarter * 32 + lane;
-            const int n0 = nb * kBN + half * 128;
-            if (m < p.M) {
-                if constexpr (kOutS32) {
+            if constexpr (kOutS32) {
+                if (m < p.M) {
                     int32_t* row = static_cast<int32_t*>(p.out) + static_cast<int64_t>(m) * p.N;
 #pragma unroll
                     for (int g = 0; g < 32; ++g) {
@@ -414,46 +444,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             *reinterpret_cast<int4*>(row + n) =
                                 make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
                     }
-                } else {
-                    const float sxm = p.sx[m];
+                }
+            } else {
+                // y = bf16_rne(((float)acc * sx[m]) * sw[n] + bias[n]), eight
+                // columns at a time, packed as four bf16 pairs.
+                const float* swc = s_sw + half * 128;
+                const float* bc = s_bias + half * 128;
+                auto dequant8 = [&](int g, uint4& out) {
+                    float y[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * g + i]), sxm), swc[8 * g + i]);
+                    if (p.bias_mode != 0) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(y[i], bc[8 * g + i]);
+                    }
+                    out = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                     pack_bf16x2(y[6], y[7]));
+                };
+                if constexpr (kPair == 2) {
+                    // Stage this warp's 32 rows x 128 columns as two 32 x 64
+                    // boxes in the 128-byte swizzle (16-byte chunk c of row r
+                    // at chunk c ^ (r % 8): conflict-free), then TMA-store
+                    // them; the store clips rows >= M and columns >= N.
+                    uint8_t* buf = sOut + e * 8192;
+                    if (lane == 0) bulk_wait_read_all();   // the previous tile's stores have read it
+                    __syncwarp();
+#pragma unroll
+                    for (int g = 0; g < 16; ++g) {
+                        uint4 v;
+                        dequant8(g, v);
+                        const int j = g >> 3, c = g & 7;
+                        *reinterpret_cast<uint4*>(buf + j * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int row0 = (mb * kPair + static_cast<int>(rank)) * kBM + quarter * 32;
+                        if (row0 < p.M) {
+                            if (n0 < p.N) tma_store_2d(&tmap_y, buf, n0, row0);
+                            if (n0 + 64 < p.N) tma_store_2d(&tmap_y, buf + 4096, n0 + 64, row0);
+                        }
+                        bulk_commit_group();
+                    }
+                } else if (m < p.M) {
                     uint16_t* row = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(m) * p.N;
 #pragma unroll
                     for (int g = 0; g < 16; ++g) {
                         const int n = n0 + g * 8;
                         if (n < p.N) {
-                            const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.sw + n));
-                            const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.sw + n + 4));
-                            const float swv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                            float y[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * g + i]), sxm), swv[i]);
-                            if (p.bias_mode == 1) {
-                                const float4 b0 = __ldg(reinterpret_cast<const float4*>(
-                                    static_cast<const float*>(p.bias) + n));
-                                const float4 b1 = __ldg(reinterpret_cast<const float4*>(
-                                    static_cast<const float*>(p.bias) + n + 4));
-                                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(y[i], bv[i]);
-                            } else if (p.bias_mode == 2) {
-                                const uint4 bb = __ldg(reinterpret_cast<const uint4*>(
-                                    static_cast<const uint16_t*>(p.bias) + n));
-                                const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    y[2 * i] = __fadd_rn(y[2 * i], __uint_as_float(bw[i] << 16));
-                                    y[2 * i + 1] = __fadd_rn(y[2 * i + 1], __uint_as_float(bw[i] & 0xFFFF0000u));
-                                }
-                            }
-                            *reinterpret_cast<uint4*>(row + n) = make_uint4(
-                                pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                pack_bf16x2(y[6], y[7]));
+                            uint4 v;
+                            dequant8(g, v);
+                            *reinterpret_cast<uint4*>(row + n) = v;
                         }
                     }
                 }
             }
         }
+        // Output stores still in flight must finish before the CTA exits.
+        if (kPair == 2 && !kOutS32 && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before_sync();

@@ -80,8 +80,9 @@ bool load_encode_fn()
     return g_encode != nullptr;
 }
 
-// 2-D bf16 tensor [rows][inner] (inner contiguous), tiles of box_rows x 64
-// elements (128 bytes) with 128-byte swizzling, zero fill out of bounds.
+// 2-D bf16 tensor [rows][inner] (inner contiguous), boxes of box_rows x 64
+// elements (128 bytes) with 128-byte swizzling; loads zero-fill outside the
+// tensor, stores skip it.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t inner, uint32_t box_rows)
 {
     if (!load_encode_fn()) return false;
@@ -336,9 +337,15 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
 {
     if (!ensure_gemm_ready(dev)) return W8A8_ERR_CUDA;
     const GemmPlan g = choose_plan(M, N, K, dev->num_sms, dev->pair_workers, slots);
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
     if (!encode_bf16_2d(&ta, A_codes, M, K, w8a8::kBM)) return W8A8_ERR_CUDA;
     if (!encode_bf16_2d(&tb, Wp, N, K, static_cast<uint32_t>(w8a8::kBN / g.pair))) return W8A8_ERR_CUDA;
+    // The pair form stores bf16 Y through TMA in 32-row x 64-column boxes.
+    if (!kOutS32 && g.pair == 2) {
+        if (!encode_bf16_2d(&ty, out, M, N, 32)) return W8A8_ERR_CUDA;
+    } else {
+        ty = tb;   // not read by these forms
+    }
     w8a8::GemmParams p;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
@@ -361,7 +368,7 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     p.tail_units = static_cast<int32_t>(g.tail_units);
     if (g.pair == 1) {
         w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 1>
-            <<<g.grid, w8a8::kGemmThreads, w8a8::GemmCfg<1>::kSmemBytes, stream>>>(ta, tb, p);
+            <<<g.grid, w8a8::kGemmThreads, w8a8::GemmCfg<1>::kSmemBytes, stream>>>(ta, tb, ty, p);
         return last_launch_status();
     }
     cudaLaunchConfig_t cfg = {};
@@ -376,7 +383,7 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 2>, ta, tb, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 2>, ta, tb, ty, p) != cudaSuccess) {
         cudaGetLastError();
         return W8A8_ERR_CUDA;
     }
