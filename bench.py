@@ -46,9 +46,8 @@ FLUSH_BYTES = 256 << 20
 # Valid only for the kernel sources it was taken on: the key is a digest of
 # them, and the bench reports null traffic when the sources have changed since.
 GEMM_SOURCES = ["w8a8_int8_linear_act_b300/csrc/gemm_tcgen05.cuh",
-                "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh",
-                "w8a8_int8_linear_act_b300/csrc/w8a8_api.cu"]
-GEMM_TRAFFIC = {"ea91e8b591ee6ab9": 163.63e6}
+                "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh"]
+GEMM_TRAFFIC = {"49926ccd378700e7": 165.92e6}
 
 
 def sources_digest(paths):
@@ -344,15 +343,19 @@ def run_ours(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
+    def step():
+        # One call of the hot path: w8a8_linear (quantiser, then the GEMM as
+        # its programmatic dependent).
+        w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=stream)
+
+    def staged(evs):
+        # The same two kernels through the two stage calls, with an event
+        # between them: each kernel's own duration (no overlap between them).
+        evs[0].record(stream)
         w8.linear_quant_stage(Xd, ws, stream=stream)
-        if evs is not None:
-            evs[1].record(stream)
+        evs[1].record(stream)
         w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)
-        if evs is not None:
-            evs[2].record(stream)
+        evs[2].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -362,7 +365,8 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError("device status %d bits %#x after warm-up" % (st, bits_))
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     try:
         pr = torch.cuda.get_device_properties(dev)
         pci = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
@@ -375,14 +379,22 @@ def run_ours(args):
         t_wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
-            step(evs[i])
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
+        barrier(world)
+        # per-kernel durations, for the rooflines (a second timed pass)
+        for i in range(args.steps):
+            flush.zero_()
+            staged(kevs[i])
+        torch.cuda.synchronize()
     barrier(world)
     launches = 2 * args.steps
-    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    g_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    s_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    s_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    q_ms = [e[0].elapsed_time(e[1]) for e in kevs]
+    g_ms = [e[1].elapsed_time(e[2]) for e in kevs]
     step_ms = max_over_ranks(statistics.mean(s_ms), world)
     gemm_ms = statistics.mean(g_ms)
     quant_ms = statistics.mean(q_ms)
@@ -390,24 +402,22 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError("device status %d bits %#x after timed steps" % (st, bits_))
 
-    # end to end through the public call, host buffers, copies inside the timed region
+    # End to end through the public C call with host buffers
+    # (w8a8_linear_host): the copy of X in and of Y out are inside the timed
+    # region, pipelined over row chunks against the compute.
     Xh = X.pin_memory()
     Yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     Xe = torch.empty_like(Xd)
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
-        Xe.copy_(Xh, non_blocking=True)
-        w8.linear(Xe, Wp, sw, bd, out=Y, workspace=ws)
-        Yh.copy_(Y, non_blocking=True)
+        w8.linear_host(Xh, Wp, sw, bd, out=Yh, X_dev=Xe, Y_dev=Y, workspace=ws, stream=stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for _ in range(e2e_steps):
         flush.zero_()
         e0.record(stream)
-        Xe.copy_(Xh, non_blocking=True)
-        w8.linear(Xe, Wp, sw, bd, out=Y, workspace=ws)
-        Yh.copy_(Y, non_blocking=True)
+        w8.linear_host(Xh, Wp, sw, bd, out=Yh, X_dev=Xe, Y_dev=Y, workspace=ws, stream=stream)
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
@@ -449,6 +459,9 @@ def run_ours(args):
                     "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
                     "d2h_bytes_per_step": Yh.numel() * Yh.element_size()},
             "gpu_launches": launches,
+            "kernel_split_ms": {"quant": quant_ms, "gemm": gemm_ms,
+                                "note": "each kernel alone (event between them); the step overlaps the "
+                                        "GEMM's set-up with the quantiser's tail"},
             "clocks": clocks,
             "wall_s_timed": t_wall,
         }

@@ -252,6 +252,36 @@ W8A8_API w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, 
                                          const void* bias, int bias_dtype, uint16_t* Y, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * w8a8_linear from and to HOST memory, pipelined over row chunks.
+ *   X_host [M][K] of `x_dtype`, host memory                 in
+ *   Y_host [M][N] bf16 bit patterns, host memory            out
+ *   X_dev  [M][K] of `x_dtype`, device staging               (caller-owned)
+ *   Y_dev  [M][N] bf16, device staging                       (caller-owned)
+ *   ws     >= w8a8_linear_workspace_min_bytes(chunk, K) for the chunk size
+ *          used (w8a8_linear_workspace_bytes(chunk, N, K) for full speed)
+ *   chunk_rows  rows per chunk; 0 = about M / 8 rounded up to 256 rows (at
+ *          most 64 chunks)
+ * Wp, sw, bias as in w8a8_linear.  For each chunk of rows: the host-to-device
+ * copy of X on a copy stream, then w8a8_linear on `stream`, then the
+ * device-to-host copy of Y on a second copy stream, so the copies of one
+ * chunk overlap the other chunks' compute and the copies in the other
+ * direction.  The whole call is ordered on `stream` like any other entry
+ * point: it starts after earlier work on `stream`, and later work on
+ * `stream` sees Y_host written.  Host buffers should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously.
+ * The library creates two copy streams and a set of events per device on
+ * the first call (no device memory) and keeps them until the process exits;
+ * make that first call before any stream capture.  Calls on one device must
+ * not overlap (they share those streams and events).  The status word in
+ * `ws` reflects the last chunk only.
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t K,
+                                      const uint16_t* Wp, const float* sw, int64_t N,
+                                      const void* bias, int bias_dtype, uint16_t* Y_host,
+                                      void* X_dev, uint16_t* Y_dev, void* ws, size_t ws_bytes,
+                                      int64_t chunk_rows, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Device status of the last call that used `ws`: synchronises `stream`,
  * copies the workspace's status word to *device_bits (host pointer) and
  * returns W8A8_OK when it is 0, W8A8_ERR_TIMEOUT when a bounded device wait

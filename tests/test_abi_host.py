@@ -184,3 +184,17 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(w8, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         w8.load()
+
+
+def test_host_pipeline_argument_errors(lib):
+    """w8a8_linear_host validates before any copy or launch (no GPU here)."""
+    p = ctypes.c_void_p(0x10000)
+    null = None
+    f = lib.w8a8_linear_host
+    assert f(null, 1, 64, 256, p, p, 128, null, 1, p, p, p, p, 1 << 20, 0, null) == 1
+    assert f(p, 1, 64, 256, p, p, 128, null, 1, null, p, p, p, 1 << 20, 0, null) == 1
+    assert f(p, 1, 64, 256, p, p, 128, null, 1, p, p, p, p, 1 << 20, -1, null) == 1
+    assert f(p, 5, 64, 256, p, p, 128, null, 1, p, p, p, p, 1 << 20, 0, null) == 2
+    assert f(p, 1, 64, 250, p, p, 128, null, 1, p, p, p, p, 1 << 20, 0, null) == 4
+    assert f(p, 1, 64, 256, p, p, 128, null, 1, p, p, p, p, 64, 0, null) == 5
+    assert f(p, 1, 64, 256, p, p, 128, null, 1, p, ctypes.c_void_p(0x10008), p, p, 1 << 20, 0, null) == 3

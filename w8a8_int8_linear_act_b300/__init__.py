@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
     "quantize_act", "pack_weight", "workspace_bytes", "workspace_min_bytes", "gemm_plan", "linear", "linear_quant_stage",
-    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
+    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "linear_host", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
     "W8A8Linear", "F32", "BF16", "MAX_K",
 ]
 
@@ -79,6 +79,7 @@ def _load():
         "w8a8_linear_gemm_stage": ([i64, i64, p, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_gemm_s32": ([p, p, i64, i64, i64, p, p, sz, p], i32),
         "w8a8_linear_noalloc": ([p, i32, i64, i64, p, p, i64, p, i32, p, p], i32),
+        "w8a8_linear_host": ([p, i32, i64, i64, p, p, i64, p, i32, p, p, p, p, sz, i64, p], i32),
         "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "w8a8_debug_skip_loads": ([i32], None),
@@ -249,6 +250,37 @@ def gemm_s32(Xq: torch.Tensor, Wp: torch.Tensor, out=None, workspace=None, strea
     ws = _workspace(M, N, K, Xq.device, workspace)
     _check(_load().w8a8_gemm_s32(_ptr(Xq), _ptr(Wp), M, N, K, _ptr(out), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)), "w8a8_gemm_s32")
+    return out
+
+
+def linear_host(X_host: torch.Tensor, Wp: torch.Tensor, sw: torch.Tensor, bias=None, out=None,
+                X_dev=None, Y_dev=None, workspace=None, chunk_rows: int = 0, stream=None) -> torch.Tensor:
+    """``linear`` from a host (CPU) X to a host Y, pipelined over row chunks:
+    each chunk's copy in, W8A8 linear and copy out overlap the other chunks'
+    (one C call, ``w8a8_linear_host``).  X_host and ``out`` should be pinned
+    (``pin_memory()``).  X_dev / Y_dev / workspace are the device staging
+    buffers (allocated here when not given).  Ordered on ``stream``."""
+    if X_host.is_cuda or X_host.dim() != 2 or not X_host.is_contiguous():
+        raise ValueError("X_host must be a contiguous 2-D CPU tensor")
+    _cuda2d(Wp, "Wp")
+    M, K = X_host.shape
+    N = Wp.shape[0]
+    dev = Wp.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+    if out.is_cuda or tuple(out.shape) != (M, N) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] bfloat16 CPU tensor")
+    if X_dev is None:
+        X_dev = torch.empty((M, K), dtype=X_host.dtype, device=dev)
+    if Y_dev is None:
+        Y_dev = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = torch.empty((workspace_bytes(M, N, K),), dtype=torch.uint8, device=dev)
+    bdt = _dt(bias) if bias is not None else BF16
+    _check(_load().w8a8_linear_host(_ptr(X_host), _dt(X_host), M, K, _ptr(Wp), _ptr(sw), N, _ptr(bias), bdt,
+                                    _ptr(out), _ptr(X_dev), _ptr(Y_dev), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), int(chunk_rows),
+                                    _stream(stream)), "w8a8_linear_host")
     return out
 
 

@@ -230,6 +230,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if constexpr (kPair == 2) cluster_sync_all();   // both CTAs' barriers exist before any remote use
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    // Launched as a programmatic dependent of the kernel that writes the
+    // activation codes, row scales and the workspace header: the set-up
+    // above overlaps its tail, nothing below may run before it completes.
+    grid_wait_prerequisites();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

@@ -6,14 +6,17 @@
 //   s==0 -> zero row: scale 1, codes 0
 //   q    = clamp(round_half_even(fp32(x / s)), -127, 127)
 //
-// One CTA per row.  The row is read once from HBM with 16-byte vector loads
-// (thread t takes vectors t, t + T, t + 2T, ... so every warp instruction
-// covers 512 contiguous bytes), held in registers while the absmax is
-// reduced (warp shuffles, then one shared-memory step across warps), then
-// quantised and written with 4/8/16-byte vector stores.  Rows too long for
-// the register budget take a second pass over the row instead (served from
-// L2).  The codes go out either as int8 (the API's codes) or as bf16 values
-// of the same integers (the tensor-core GEMM's operand).
+// Structure.  A row is read once from HBM with 16-byte vector loads (thread
+// t of the row's T threads takes vectors t, t + T, t + 2T, ..., so every warp
+// instruction covers 512 contiguous bytes) and held in registers while its
+// absmax is reduced, then quantised and written with 8/16-byte vector
+// stores.  Rows of up to 512 vectors (K <= 4096 for bf16, 2048 for fp32) take
+// one warp each, four rows per CTA, reduced with warp shuffles alone; rows of
+// up to 4096 vectors take a CTA of up to 256 threads with 16 vectors each
+// (shuffles, then one shared-memory step).  Longer rows take a second pass
+// over the row instead of holding it (served from L2).  The codes go out either as int8 (the API's
+// codes) or as bf16 values of the same integers (the tensor-core GEMM's
+// operand).
 //
 // Exact codes without a division per element.  With r = fp32(1/s) (correctly
 // rounded) and v = fp32(x * r), |v - x/s| <= |x/s| * (2^-24 + 2^-24 + 2^-48)
@@ -22,7 +25,10 @@
 // every half-integer, v and fp32(x/s) lie strictly inside the same interval
 // (n - 1/2, n + 1/2) and round to the same integer n.  Only elements closer
 // than that to a tie (about one in 8000 for smooth data), and rows whose
-// reciprocal overflows (s below 2^-128), take the IEEE division.  The
+// reciprocal overflows (s below 2^-128), take the IEEE division.  The test is
+// made once per 16-byte vector (the largest distance of its elements from
+// their rounded values), and the division sits behind that one branch, so
+// the common path pays no part of it.  The
 // rounding to an integer adds 1.5 * 2^23: for |v| < 2^22 the fp32 sum has a
 // unit in the last place of exactly 1, so round-to-nearest-even of the add
 // is round-half-even of v (the classic magic-number rounding).  In the fast
@@ -31,6 +37,8 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+
+#include "ptx_sm103.cuh"
 
 namespace w8a8 {
 
@@ -94,48 +102,31 @@ struct InVec<float> {
 struct RowScale {
     float s;        // scale (1 for a zero row)
     float r;        // fp32(1 / s)
-    bool zero;      // zero row: all codes 0
     bool exact;     // reciprocal overflowed: every element takes the division
 };
 
+// A zero row (amax / 127 == 0, including an fp32 amax that underflows) gets
+// s = 1; its elements are all zero or so small that x * 1 rounds to code 0.
 __device__ __forceinline__ RowScale row_scale(float amax)
 {
     RowScale rs;
     const float s = __fdiv_rn(amax, 127.0f);
-    rs.zero = (s == 0.0f);
-    rs.s = rs.zero ? 1.0f : s;
+    rs.s = (s == 0.0f) ? 1.0f : s;
     rs.r = __frcp_rn(rs.s);
     rs.exact = !(fabsf(rs.r) <= 3.402823466e38f);
     return rs;
 }
 
-// The code of x as the fp32 value kRoundMagic + q (q in [-127, 127]).
-__device__ __forceinline__ float code_biased(float x, const RowScale& rs)
-{
-    const float v = __fmul_rn(x, rs.r);
-    float t = __fadd_rn(v, kRoundMagic);
-    const float f = __fsub_rn(v, __fsub_rn(t, kRoundMagic));
-    if (rs.exact || fabsf(f) > kNearHalf) {
-        const float q = __fdiv_rn(x, rs.s);
-        t = __fadd_rn(fminf(fmaxf(q, -127.0f), 127.0f), kRoundMagic);
-    }
-    return rs.zero ? kRoundMagic : t;
-}
-
-// Writes E codes given as biased floats, at element offset `off`.
+// Writes E codes given as integer-valued floats q, at element offset `off`.
 template <bool kBf16Codes, int E>
-__device__ __forceinline__ void store_codes(void* Q, int64_t off, const float (&t)[E])
+__device__ __forceinline__ void store_codes(void* Q, int64_t off, const float (&q)[E])
 {
     if constexpr (kBf16Codes) {
         // bf16 of the integer q is the top half of fp32(q): |q| <= 127 needs
         // at most 8 significant bits, so the truncation is exact.
         uint32_t w[E / 2];
 #pragma unroll
-        for (int i = 0; i < E / 2; ++i) {
-            const float q0 = __fsub_rn(t[2 * i], kRoundMagic);
-            const float q1 = __fsub_rn(t[2 * i + 1], kRoundMagic);
-            w[i] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
-        }
+        for (int i = 0; i < E / 2; ++i) w[i] = __byte_perm(__float_as_uint(q[2 * i]), __float_as_uint(q[2 * i + 1]), 0x7632);
         uint16_t* dst = static_cast<uint16_t*>(Q) + off;
         if constexpr (E == 8)
             *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -144,11 +135,14 @@ __device__ __forceinline__ void store_codes(void* Q, int64_t off, const float (&
     } else {
         // The low byte of bits(kRoundMagic + q) is q's two's-complement byte
         // (kRoundMagicBits has a zero low byte and |q| < 2^22).
+        uint32_t b[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) b[i] = __float_as_uint(__fadd_rn(q[i], kRoundMagic));
         uint32_t w[E / 4];
 #pragma unroll
         for (int i = 0; i < E / 4; ++i) {
-            const uint32_t p01 = __byte_perm(__float_as_uint(t[4 * i]), __float_as_uint(t[4 * i + 1]), 0x0040);
-            const uint32_t p23 = __byte_perm(__float_as_uint(t[4 * i + 2]), __float_as_uint(t[4 * i + 3]), 0x0040);
+            const uint32_t p01 = __byte_perm(b[4 * i], b[4 * i + 1], 0x0040);
+            const uint32_t p23 = __byte_perm(b[4 * i + 2], b[4 * i + 3], 0x0040);
             w[i] = __byte_perm(p01, p23, 0x5410);
         }
         int8_t* dst = static_cast<int8_t*>(Q) + off;
@@ -168,11 +162,17 @@ __device__ __forceinline__ uint4 load_stream(const uint4* p)
     return v;
 }
 
-// Block-wide max of non-negative values; every thread gets the result.
-__device__ __forceinline__ float block_max(float v, float* red /* >= 32 floats */)
+__device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Block-wide max of non-negative values; every thread gets the result.
+__device__ __forceinline__ float block_max(float v, float* red /* >= 32 floats */)
+{
+    v = warp_max(v);
     const int nwarps = blockDim.x >> 5;
     if (nwarps == 1) return v;
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
@@ -182,74 +182,112 @@ __device__ __forceinline__ float block_max(float v, float* red /* >= 32 floats *
     return m;
 }
 
+// round_half_even(clamp(fp32(x / s), -127, 127)) by IEEE division.  Out of
+// line: it runs only for elements within 2^-14 of a tie, and inlining its
+// code at every element would crowd the instruction cache.
+__device__ __noinline__ float code_by_division(float x, float s)
+{
+    const float d = fminf(fmaxf(__fdiv_rn(x, s), -127.0f), 127.0f);
+    return __fsub_rn(__fadd_rn(d, kRoundMagic), kRoundMagic);
+}
+
+// Codes of one 16-byte vector.  Fast path: v = x * r rounded half-to-even by
+// the magic add; if any element of the vector lies within 2^-14 of a tie (or
+// the row needs exact division), that element is redone with the IEEE
+// quotient fp32(x / s), clamped to [-127, 127].
 template <typename TIn, bool kBf16Codes>
-__device__ __forceinline__ void quantize_vector(const uint4& v, const RowScale& rs, void* Q, int64_t off)
+__device__ __forceinline__ void quantize_vector(const uint4& vec, const RowScale& rs, void* Q, int64_t off)
 {
     using IV = InVec<TIn>;
     constexpr int E = IV::kElems;
-    float f[E];
-    IV::unpack(v, f);
-    float t[E];
+    float x[E];
+    IV::unpack(vec, x);
+    float q[E];
+    float dmax = 0.0f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) t[e] = code_biased(f[e], rs);
-    store_codes<kBf16Codes, E>(Q, off, t);
+    for (int e = 0; e < E; ++e) {
+        const float v = __fmul_rn(x[e], rs.r);
+        q[e] = __fsub_rn(__fadd_rn(v, kRoundMagic), kRoundMagic);
+        dmax = fmaxf(dmax, fabsf(__fsub_rn(v, q[e])));
+    }
+    if (dmax > kNearHalf || rs.exact) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float v = __fmul_rn(x[e], rs.r);
+            if (rs.exact || fabsf(__fsub_rn(v, q[e])) > kNearHalf) q[e] = code_by_division(x[e], rs.s);
+        }
+    }
+    store_codes<kBf16Codes, E>(Q, off, q);
 }
 
+// Rows of A [R][K] -> codes Q [R][K] and scales S [R].
+//   kRowsPerCta > 1: blockDim.x == 32 * kRowsPerCta, warp w takes row
+//                    blockIdx.x * kRowsPerCta + w (rows past R do nothing);
+//   kRowsPerCta == 1: the whole CTA takes row blockIdx.x.
 // NV > 0: each thread keeps up to NV vectors of the row in registers (single
 // HBM read).  NV == 0: two passes over the row (for very long rows).
-// `status`, when not NULL, is the workspace header (status word and the
+// `header`, when not NULL, is the workspace header (status word and the
 // GEMM's split-tile counters), cleared by block 0 at the start of a call.
-template <typename TIn, bool kBf16Codes, int NV>
-__global__ void __launch_bounds__(1024) quant_rows_kernel(const TIn* __restrict__ A, int64_t K,
+template <typename TIn, bool kBf16Codes, int NV, int kRowsPerCta>
+__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ? 256 : 1024)) quant_rows_kernel(const TIn* __restrict__ A, int64_t R, int64_t K,
                                                           void* __restrict__ Q, float* __restrict__ S,
-                                                          uint32_t* __restrict__ status)
+                                                          uint32_t* __restrict__ header)
 {
     using IV = InVec<TIn>;
     constexpr int E = IV::kElems;
     __shared__ float red[32];
 
-    const int64_t row = blockIdx.x;
+    // The GEMM that follows may be scheduled as soon as every CTA of this
+    // grid is resident; it waits for this grid's results before reading.
+    grid_launch_dependents();
+    if (header != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
+
+    const int64_t row = kRowsPerCta > 1 ? static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5)
+                                        : static_cast<int64_t>(blockIdx.x);
+    if (kRowsPerCta > 1 && row >= R) return;   // warp-uniform; no block-wide barrier follows
+    const int T = kRowsPerCta > 1 ? 32 : static_cast<int>(blockDim.x);
+    const int t = kRowsPerCta > 1 ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
     const int V = static_cast<int>(K / E);  // 16-byte vectors in the row (K % 16 == 0)
     const uint4* src = reinterpret_cast<const uint4*>(A + row * K);
     const int64_t out0 = row * K;
-    const int T = blockDim.x;
-
-    if (status != nullptr && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) status[i] = 0u;
 
     uint32_t m2 = 0;
     if constexpr (NV > 0) {
         uint4 v[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-            const int idx = threadIdx.x + i * T;
+            const int idx = t + i * T;
             v[i] = (idx < V) ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
-        const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red));
-        if (threadIdx.x == 0) S[row] = rs.s;
+        const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
+        const RowScale rs = row_scale(amax);
+        if (t == 0) S[row] = rs.s;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-            const int idx = threadIdx.x + i * T;
+            const int idx = t + i * T;
             if (idx < V) quantize_vector<TIn, kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * E);
         }
     } else {
-        for (int idx = threadIdx.x; idx < V; idx += T) IV::absmax(load_stream(src + idx), m2);
-        const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red));
-        if (threadIdx.x == 0) S[row] = rs.s;
-        for (int idx = threadIdx.x; idx < V; idx += T)
+        for (int idx = t; idx < V; idx += T) IV::absmax(load_stream(src + idx), m2);
+        const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
+        const RowScale rs = row_scale(amax);
+        if (t == 0) S[row] = rs.s;
+        for (int idx = t; idx < V; idx += T)
             quantize_vector<TIn, kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
     }
 }
 
 // int8 codes -> the same integers as bf16 (exact), 16 codes per thread step.
-// `status`, when not NULL, is the workspace header, cleared by block 0.
+// `header`, when not NULL, is the workspace header, cleared by block 0.
 __global__ void codes_to_bf16_kernel(const int8_t* __restrict__ Qi, uint16_t* __restrict__ Qb, int64_t n16,
-                                     uint32_t* __restrict__ status)
+                                     uint32_t* __restrict__ header)
 {
-    if (status != nullptr && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) status[i] = 0u;
+    grid_launch_dependents();
+    if (header != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
     const uint4* src = reinterpret_cast<const uint4*>(Qi);
     uint4* dst = reinterpret_cast<uint4*>(Qb);
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;

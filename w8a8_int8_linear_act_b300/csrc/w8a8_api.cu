@@ -260,28 +260,40 @@ w8a8_status last_launch_status()
 
 // ---------------------------------------------------------------- row quant
 
+template <typename TIn, bool kBf16Codes, int NV, int kRows>
+void launch_quant_cfg(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header, unsigned threads,
+                      cudaStream_t stream)
+{
+    const int64_t blocks = (R + kRows - 1) / kRows;
+    w8a8::quant_rows_kernel<TIn, kBf16Codes, NV, kRows>
+        <<<static_cast<unsigned>(blocks), threads, 0, stream>>>(A, R, K, Q, S, header);
+}
+
+// Rows of up to 512 16-byte vectors: a warp per row, four rows per CTA, each
+// lane holding up to 16 vectors.  Up to 4096 vectors: a CTA per row of
+// ceil(V / 16) threads rounded to warps.  Longer: a CTA of 1024 threads per
+// row reading it twice.
 template <typename TIn, bool kBf16Codes>
-w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* status,
+w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header,
                                cudaStream_t stream)
 {
     constexpr int E = w8a8::InVec<TIn>::kElems;
     const int64_t V = K / E;  // vectors per row
-    // Threads per row: enough that each holds at most 4 vectors, 32..1024.
-    int64_t T = 32;
-    while (T < 1024 && T * 4 < V) T *= 2;
-    const int64_t per = (V + T - 1) / T;
-    const dim3 grid(static_cast<unsigned>(R));
-    const dim3 block(static_cast<unsigned>(T));
-    if (per <= 1)
-        w8a8::quant_rows_kernel<TIn, kBf16Codes, 1><<<grid, block, 0, stream>>>(A, K, Q, S, status);
-    else if (per <= 2)
-        w8a8::quant_rows_kernel<TIn, kBf16Codes, 2><<<grid, block, 0, stream>>>(A, K, Q, S, status);
-    else if (per <= 4)
-        w8a8::quant_rows_kernel<TIn, kBf16Codes, 4><<<grid, block, 0, stream>>>(A, K, Q, S, status);
-    else if (per <= 8)
-        w8a8::quant_rows_kernel<TIn, kBf16Codes, 8><<<grid, block, 0, stream>>>(A, K, Q, S, status);
-    else
-        w8a8::quant_rows_kernel<TIn, kBf16Codes, 0><<<grid, block, 0, stream>>>(A, K, Q, S, status);
+    if (V <= 32)
+        launch_quant_cfg<TIn, kBf16Codes, 1, 4>(A, R, K, Q, S, header, 128, stream);
+    else if (V <= 64)
+        launch_quant_cfg<TIn, kBf16Codes, 2, 4>(A, R, K, Q, S, header, 128, stream);
+    else if (V <= 128)
+        launch_quant_cfg<TIn, kBf16Codes, 4, 4>(A, R, K, Q, S, header, 128, stream);
+    else if (V <= 256)
+        launch_quant_cfg<TIn, kBf16Codes, 8, 4>(A, R, K, Q, S, header, 128, stream);
+    else if (V <= 512)
+        launch_quant_cfg<TIn, kBf16Codes, 16, 4>(A, R, K, Q, S, header, 128, stream);
+    else if (V <= 4096) {
+        const unsigned T = static_cast<unsigned>(((V + 15) / 16 + 31) / 32 * 32);
+        launch_quant_cfg<TIn, kBf16Codes, 16, 1>(A, R, K, Q, S, header, T, stream);
+    } else
+        launch_quant_cfg<TIn, kBf16Codes, 0, 1>(A, R, K, Q, S, header, 1024, stream);
     return last_launch_status();
 }
 
@@ -366,28 +378,71 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     p.dp_tiles = static_cast<int32_t>(g.dp_tiles);
     p.splits = g.splits;
     p.tail_units = static_cast<int32_t>(g.tail_units);
-    if (g.pair == 1) {
-        w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 1>
-            <<<g.grid, w8a8::kGemmThreads, w8a8::GemmCfg<1>::kSmemBytes, stream>>>(ta, tb, ty, p);
-        return last_launch_status();
-    }
+    // A programmatic dependent of the kernel before it in the stream (the
+    // quantiser that writes its codes): its set-up overlaps that kernel's
+    // tail, and it waits on the device for its results (griddepcontrol).
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(g.grid));
     cfg.blockDim = dim3(w8a8::kGemmThreads);
-    cfg.dynamicSmemBytes = w8a8::GemmCfg<2>::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 2>, ta, tb, ty, p) != cudaSuccess) {
+    cudaError_t err;
+    if (g.pair == 1) {
+        cfg.dynamicSmemBytes = w8a8::GemmCfg<1>::kSmemBytes;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 1>, ta, tb, ty, p);
+    } else {
+        cfg.dynamicSmemBytes = w8a8::GemmCfg<2>::kSmemBytes;
+        cfg.numAttrs = 2;
+        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 2>, ta, tb, ty, p);
+    }
+    if (err != cudaSuccess) {
         cudaGetLastError();
         return W8A8_ERR_CUDA;
     }
     return last_launch_status();
+}
+
+// Copy streams and events of w8a8_linear_host, created once per device (with
+// that device current) and kept until the process exits.  Streams and events
+// are not device memory; the entry point itself allocates nothing.
+constexpr int kMaxHostChunks = 64;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t copied[kMaxHostChunks] = {};
+    cudaEvent_t computed[kMaxHostChunks] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mutex;
+
+HostPipe* host_pipe(int dev)
+{
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe& hp = g_pipe[dev];
+    if (hp.ready) return &hp;
+    const unsigned ef = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.end, ef) == cudaSuccess;
+    for (int i = 0; ok && i < kMaxHostChunks; ++i)
+        ok = cudaEventCreateWithFlags(&hp.copied[i], ef) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp.computed[i], ef) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return nullptr;   // leaves what was created; a later call retries the rest
+    }
+    hp.ready = true;
+    return &hp;
 }
 
 // Scratch for w8a8_linear_noalloc: a workspace built into the library for
@@ -587,6 +642,71 @@ w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K
     }
     return w8a8_linear(X, x_dtype, M, K, Wp, sw, N, bias, bias_dtype, Y, scratch, W8A8_NOALLOC_SCRATCH_BYTES,
                        stream);
+}
+
+w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp,
+                             const float* sw, int64_t N, const void* bias, int bias_dtype, uint16_t* Y_host,
+                             void* X_dev, uint16_t* Y_dev, void* ws, size_t ws_bytes, int64_t chunk_rows,
+                             void* stream)
+{
+    if (!X_host || !Y_host || !X_dev || !Y_dev || !Wp || !sw || M < 0 || N < 0 || K < 0 || chunk_rows < 0)
+        return W8A8_ERR_INVALID_ARG;
+    if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (bias && bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (guard_reasons(M, N, K, x_dtype, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    // Row chunks: the copies of one chunk overlap the other chunks' compute
+    // and copies in the other direction.  Default: about eight chunks of
+    // whole 256-row tiles.
+    int64_t rows = chunk_rows;
+    if (rows == 0) rows = ((M + 7) / 8 + 255) / 256 * 256;
+    if ((M + rows - 1) / rows > kMaxHostChunks) rows = (M + kMaxHostChunks - 1) / kMaxHostChunks;
+    WsLayout L;
+    if (!ws || !ws_layout(rows < M ? rows : M, K, &L) || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(X_dev, 16) || !aligned(Y_dev, 16) || !aligned(Wp, 16) || !aligned(sw, 16) || !aligned(ws, 16))
+        return W8A8_ERR_ALIGNMENT;
+    if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
+    int dev = -1;
+    if (!device_info(&dev)) return W8A8_ERR_NO_DEVICE;
+    HostPipe* hp = host_pipe(dev);
+    if (!hp) return W8A8_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t xe = x_dtype == W8A8_BF16 ? 2u : 4u;
+    const size_t x_row = static_cast<size_t>(K) * xe, y_row = static_cast<size_t>(N) * 2u;
+    auto fail = [](cudaError_t e) { return e != cudaSuccess; };
+    // The copies start after the caller's earlier work on `stream` (which
+    // may still use X_dev / Y_dev).
+    if (fail(cudaEventRecord(hp->start, s)) || fail(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+        fail(cudaStreamWaitEvent(hp->d2h, hp->start, 0))) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    int c = 0;
+    for (int64_t r0 = 0; r0 < M; r0 += rows, ++c) {
+        const int64_t mr = (M - r0) < rows ? (M - r0) : rows;
+        const uint8_t* xh = static_cast<const uint8_t*>(X_host) + static_cast<size_t>(r0) * x_row;
+        uint8_t* xd = static_cast<uint8_t*>(X_dev) + static_cast<size_t>(r0) * x_row;
+        uint16_t* yd = Y_dev + static_cast<size_t>(r0) * static_cast<size_t>(N);
+        uint16_t* yh = Y_host + static_cast<size_t>(r0) * static_cast<size_t>(N);
+        if (fail(cudaMemcpyAsync(xd, xh, static_cast<size_t>(mr) * x_row, cudaMemcpyHostToDevice, hp->h2d)) ||
+            fail(cudaEventRecord(hp->copied[c], hp->h2d)) || fail(cudaStreamWaitEvent(s, hp->copied[c], 0))) {
+            cudaGetLastError();
+            return W8A8_ERR_CUDA;
+        }
+        const w8a8_status st = w8a8_linear(xd, x_dtype, mr, K, Wp, sw, N, bias, bias_dtype, yd, ws, ws_bytes, s);
+        if (st != W8A8_OK) return st;
+        if (fail(cudaEventRecord(hp->computed[c], s)) || fail(cudaStreamWaitEvent(hp->d2h, hp->computed[c], 0)) ||
+            fail(cudaMemcpyAsync(yh, yd, static_cast<size_t>(mr) * y_row, cudaMemcpyDeviceToHost, hp->d2h))) {
+            cudaGetLastError();
+            return W8A8_ERR_CUDA;
+        }
+    }
+    // Later work on `stream` sees Y_host complete.
+    if (fail(cudaEventRecord(hp->end, hp->d2h)) || fail(cudaStreamWaitEvent(s, hp->end, 0))) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    return W8A8_OK;
 }
 
 w8a8_status w8a8_read_status(const void* ws, void* stream, uint32_t* device_bits)
