@@ -37,7 +37,7 @@ WORKLOAD = "video"
 FLUSH_BYTES = 256 << 20
 
 # Algorithmic bytes per unit, for the rooflines:
-#   quant kernel per activation element: 2 B read (bf16) + 2 B written (bf16 code) ; + 8 B per row (scale)
+#   quant kernel per activation element: 2 B read (bf16; 4 B for fp32) + 2 B written (bf16 code); + 4 B per row (scale)
 #   GEMM per launch: codes A (2 M K) + codes B (2 N K) + sx (4 M) + sw (4 N) + bias (2 N) + Y (2 M N)
 
 
@@ -235,11 +235,16 @@ def oracle_inputs(case, X, W, b):
 
     import oracle
 
-    def u16(t):
-        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    def host(t):
+        # bf16 as its bit patterns (uint16), fp32 as is: the oracle's two input forms
+        t = t.contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
 
-    Wq, sw = oracle.quantize_rows(u16(W))
-    return u16(X), Wq, sw, oracle.bf16_bits_to_f32(u16(b))
+    Wq, sw = oracle.quantize_rows(host(W))
+    bias = host(b)
+    return host(X), Wq, sw, oracle.bf16_bits_to_f32(bias) if bias.dtype == np.uint16 else bias
 
 
 def calibrate_rows(case, inputs, target_s: float) -> int:
@@ -426,7 +431,7 @@ def run_ours(args):
     ops = case.ops
     pk = peaks()
     gemm_tflops = ops / (gemm_ms * 1e-3) / 1e12
-    quant_bytes = M * K * 2 + M * K * 2 + M * 4
+    quant_bytes = M * K * X.element_size() + M * K * 2 + M * 4
     gemm_bytes = 2 * M * K + 2 * N * K + 4 * M + 4 * N + 2 * N + 2 * M * N
     quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
     clocks = sampler.summary()
