@@ -20,7 +20,7 @@
 //              issues tcgen05.mma.cta_group::1 128x256x16.
 //   kPair = 2  a cluster of two CTAs owns a 256 x 256 tile; each CTA loads
 //              its 128 rows of A and 128 of the 256 rows of B (32 KB,
-//              6-stage ring), and the even CTA issues tcgen05.mma.cta_group::2
+//              5-stage ring), and the even CTA issues tcgen05.mma.cta_group::2
 //              256x256x16, which reads both CTAs' shared memory and leaves
 //              each CTA's 128 rows of the accumulator in its own tensor
 //              memory.  Per SM this moves 2/3 of the operand bytes of the
@@ -80,11 +80,13 @@ struct GemmCfg {
     static constexpr uint32_t kAStageBytes = kBM * kBK * 2;
     static constexpr uint32_t kBStageBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
-    static constexpr int kStages = 4;
-    // Pair form: the bf16 output tile is staged in shared memory (per
-    // epilogue warp two 32-row x 64-column boxes, 128-byte swizzled) and
-    // written by TMA stores.
-    static constexpr uint32_t kStagingBytes = kPair == 2 ? kEpiWarps * 2 * 4096 : 0;
+    static constexpr int kStages = kPair == 2 ? 5 : 4;
+    // Pair form: a 5-stage ring (the ring depth is what keeps the tensor
+    // pipe fed: 3 stages ran 170 us, 4 stages 150 us, 5 stages 139 us on the
+    // 6144 x 4096 x 4096 projection), and the bf16 output staged in shared
+    // memory, one 32-row x 64-column 128-byte-swizzled box per epilogue warp
+    // at a time, written by TMA stores.
+    static constexpr uint32_t kStagingBytes = kPair == 2 ? kEpiWarps * 4096 : 0;
     static constexpr uint32_t kParamBytes = 2 * kBN * 4;            // the tile's sw and bias, fp32
     static constexpr size_t kSmemBytes =
         1024 /* alignment slack */ + kStages * kStageBytes + kStagingBytes + kParamBytes + 256 /* barriers */;
@@ -162,10 +164,12 @@ __device__ __forceinline__ void epi_barrier()
     asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(32 * kEpiWarps) : "memory");
 }
 
+// Two floats rounded to bf16 (nearest, ties to even) in one instruction;
+// `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 template <bool kOutS32, int kPair>
@@ -455,41 +459,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float* swc = s_sw + half * 128;
                 const float* bc = s_bias + half * 128;
                 auto dequant8 = [&](int g, uint4& out) {
+                    const float4 w0 = *reinterpret_cast<const float4*>(swc + 8 * g);
+                    const float4 w1 = *reinterpret_cast<const float4*>(swc + 8 * g + 4);
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                     float y[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * g + i]), sxm), swc[8 * g + i]);
+                        y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * g + i]), sxm), wv[i]);
                     if (p.bias_mode != 0) {
+                        const float4 b0 = *reinterpret_cast<const float4*>(bc + 8 * g);
+                        const float4 b1 = *reinterpret_cast<const float4*>(bc + 8 * g + 4);
+                        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(y[i], bc[8 * g + i]);
+                        for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(y[i], bv[i]);
                     }
                     out = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                                      pack_bf16x2(y[6], y[7]));
                 };
                 if constexpr (kPair == 2) {
                     // Stage this warp's 32 rows x 128 columns as two 32 x 64
-                    // boxes in the 128-byte swizzle (16-byte chunk c of row r
-                    // at chunk c ^ (r % 8): conflict-free), then TMA-store
-                    // them; the store clips rows >= M and columns >= N.
-                    uint8_t* buf = sOut + e * 8192;
-                    if (lane == 0) bulk_wait_read_all();   // the previous tile's stores have read it
-                    __syncwarp();
+                    // boxes, one after the other in the warp's 4 KB buffer, in
+                    // the 128-byte swizzle (16-byte chunk c of row r at chunk
+                    // c ^ (r % 8): conflict-free), each TMA-stored as soon as
+                    // written; the store clips rows >= M and columns >= N.
+                    // Before a box is rewritten, the store that read it last
+                    // must have finished reading.
+                    uint8_t* buf = sOut + e * 4096;
+                    const int row0 = (mb * kPair + static_cast<int>(rank)) * kBM + quarter * 32;
 #pragma unroll
-                    for (int g = 0; g < 16; ++g) {
-                        uint4 v;
-                        dequant8(g, v);
-                        const int j = g >> 3, c = g & 7;
-                        *reinterpret_cast<uint4*>(buf + j * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const int row0 = (mb * kPair + static_cast<int>(rank)) * kBM + quarter * 32;
-                        if (row0 < p.M) {
-                            if (n0 < p.N) tma_store_2d(&tmap_y, buf, n0, row0);
-                            if (n0 + 64 < p.N) tma_store_2d(&tmap_y, buf + 4096, n0 + 64, row0);
+                    for (int j = 0; j < 2; ++j) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint4 v;
+                            dequant8(j * 8 + c, v);
+                            *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
                         }
-                        bulk_commit_group();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (row0 < p.M && n0 + 64 * j < p.N) tma_store_2d(&tmap_y, buf, n0 + 64 * j, row0);
+                            bulk_commit_group();
+                        }
                     }
                 } else if (m < p.M) {
                     uint16_t* row = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(m) * p.N;
