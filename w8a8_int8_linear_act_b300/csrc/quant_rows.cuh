@@ -18,21 +18,23 @@
 // codes) or as bf16 values of the same integers (the tensor-core GEMM's
 // operand).
 //
-// Exact codes without a division per element.  With r = fp32(1/s) (correctly
-// rounded) and v = fp32(x * r), |v - x/s| <= |x/s| * (2^-24 + 2^-24 + 2^-48)
-// <= 2^-16 for |x/s| <= 128, and the fp32 quotient itself is within 2^-18 of
-// x/s, so |v - fp32(x/s)| < 2^-15.  Whenever v is further than 2^-14 from
-// every half-integer, v and fp32(x/s) lie strictly inside the same interval
-// (n - 1/2, n + 1/2) and round to the same integer n.  Only elements closer
-// than that to a tie (about one in 8000 for smooth data), and rows whose
-// reciprocal overflows (s below 2^-128), take the IEEE division.  The test is
-// made once per 16-byte vector (the largest distance of its elements from
-// their rounded values), and the division sits behind that one branch, so
-// the common path pays no part of it.  The
-// rounding to an integer adds 1.5 * 2^23: for |v| < 2^22 the fp32 sum has a
-// unit in the last place of exactly 1, so round-to-nearest-even of the add
-// is round-half-even of v (the classic magic-number rounding).  In the fast
-// path |v| <= 127 * (1 + 2^-20), so no clamp is needed there.
+// Exact codes without a division per element.  With r = fp32(1/s)
+// (correctly rounded) and p = x * r the exact product, |p - x/s| <=
+// |x/s| * 2^-24 < 2^-17 for |x/s| <= 127.5, and the fp32 quotient fp32(x/s)
+// is within 2^-18 of x/s, so |p - fp32(x/s)| < 2^-16.  One fused multiply-add
+// t = fma(x, r, 1.5 * 2^23) rounds p + 1.5 * 2^23 once; for |p| < 2^22 that
+// sum has a unit in the last place of exactly 1, so q = t - 1.5 * 2^23 is
+// round_half_even(p) (the classic magic-number rounding, with the product
+// never rounded on its own).  A second fma gives d = fp32(p - q) (relative
+// error 2^-24).  Whenever |d| <= 1/2 - 2^-14, p lies more than
+// 2^-14 - 2^-24 > 2^-16 inside (q - 1/2, q + 1/2), so fp32(x/s) lies strictly
+// inside it too and rounds to the same q.  Only elements closer than that
+// to a tie (about one in 8000 for smooth data), and rows whose reciprocal
+// overflows (s below 2^-128), take the IEEE division.  The test is made
+// once per 16-byte vector (the largest |d| of its elements), and the
+// division sits behind that one branch in an out-of-line function, so the
+// common path pays no part of it.  In the fast path |p| <= 127 * (1 + 2^-22),
+// so no clamp is needed there.
 #pragma once
 
 #include <cstdint>
@@ -191,10 +193,10 @@ __device__ __noinline__ float code_by_division(float x, float s)
     return __fsub_rn(__fadd_rn(d, kRoundMagic), kRoundMagic);
 }
 
-// Codes of one 16-byte vector.  Fast path: v = x * r rounded half-to-even by
-// the magic add; if any element of the vector lies within 2^-14 of a tie (or
-// the row needs exact division), that element is redone with the IEEE
-// quotient fp32(x / s), clamped to [-127, 127].
+// Codes of one 16-byte vector.  Fast path: x * r rounded half-to-even by one
+// fused multiply-add with the magic constant; if any element of the vector
+// lies within 2^-14 of a tie (or the row needs exact division), that element
+// is redone with the IEEE quotient fp32(x / s), clamped to [-127, 127].
 template <typename TIn, bool kBf16Codes>
 __device__ __forceinline__ void quantize_vector(const uint4& vec, const RowScale& rs, void* Q, int64_t off)
 {
@@ -206,16 +208,13 @@ __device__ __forceinline__ void quantize_vector(const uint4& vec, const RowScale
     float dmax = 0.0f;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        const float v = __fmul_rn(x[e], rs.r);
-        q[e] = __fsub_rn(__fadd_rn(v, kRoundMagic), kRoundMagic);
-        dmax = fmaxf(dmax, fabsf(__fsub_rn(v, q[e])));
+        q[e] = __fsub_rn(__fmaf_rn(x[e], rs.r, kRoundMagic), kRoundMagic);
+        dmax = fmaxf(dmax, fabsf(__fmaf_rn(x[e], rs.r, -q[e])));
     }
     if (dmax > kNearHalf || rs.exact) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const float v = __fmul_rn(x[e], rs.r);
-            if (rs.exact || fabsf(__fsub_rn(v, q[e])) > kNearHalf) q[e] = code_by_division(x[e], rs.s);
-        }
+        for (int e = 0; e < E; ++e)
+            if (rs.exact || fabsf(__fmaf_rn(x[e], rs.r, -q[e])) > kNearHalf) q[e] = code_by_division(x[e], rs.s);
     }
     store_codes<kBf16Codes, E>(Q, off, q);
 }
