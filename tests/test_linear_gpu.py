@@ -205,3 +205,32 @@ def test_linear_pair_and_single_cta_forms_identical(cuda_device):
         w8.debug_force_single_cta(False)
     torch.cuda.synchronize()
     assert torch.equal(pair.view(torch.int16), single.view(torch.int16))
+
+
+@pytest.mark.parametrize("case,M,N,K", [
+    ("video", 1000, 520, 1024),         # ragged tiles, CTA pairs
+    ("video", 6144, 4096, 4096),        # the benchmark's layer
+    ("tiny", 64, 128, 256),             # fp32 activations, single-CTA form
+    ("audio_m126_n2048", 126, 2048, 2048),
+    ("audio_m1001_n8192", 1001, 8192, 2048),
+])
+def test_linear_repeated_calls_equal_stage_calls(cuda_device, case, M, N, K):
+    """Twenty w8a8_linear calls in a row on one workspace must each give the
+    bytes of the two stage calls (quantiser kernel, then GEMM) on the same
+    inputs, with a clean status word: the workspace header (status word,
+    split-tile counters) is cleared by every call's first kernel, and the
+    GEMM, launched as that kernel's programmatic dependent, waits for it."""
+    dev = cuda_device
+    X, W, b = wl.make(case, M=M, N=N, K=K)
+    Xd, bd = X.to(dev), b.to(dev)
+    Wq, sw = w8.quantize_weight(W.to(dev))
+    Wp = w8.pack_weight(Wq)
+    ws = torch.empty(w8.workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    w8.linear_quant_stage(Xd, ws)
+    w8.linear_gemm_stage(M, K, Wp, sw, bd, ref, ws)
+    outs = [w8.linear(Xd, Wp, sw, bd, workspace=ws) for _ in range(20)]
+    assert w8.read_status(ws) == (0, 0)
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), "call %d differs" % i
