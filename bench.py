@@ -407,6 +407,58 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError("device status %d bits %#x after timed steps" % (st, bits_))
 
+    # The same step replayed from a CUDA graph (flush + w8a8_linear captured
+    # once): GPU time alone, without the binding's per-call host work, which
+    # dominates the event intervals of the small audio shapes.
+    graph = {"value": None, "ms_per_step": None}
+    try:
+        g = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            step_on = lambda: w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=gs)  # noqa: E731
+            flush.zero_()
+            step_on()
+            gs.synchronize()
+            with torch.cuda.graph(g, stream=gs):
+                flush.zero_()
+                step_on()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(args.steps, 500))]
+        cur = torch.cuda.current_stream()
+        for a, b_ in gev:
+            a.record(cur)
+            g.replay()
+            b_.record(cur)
+        torch.cuda.synchronize()
+        g_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in gev)
+        # the captured step includes the 256 MiB flush: time it alone the same way
+        fg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(fg, stream=gs):
+                flush.zero_()
+        torch.cuda.synchronize()
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+        for a, b_ in fev:
+            a.record(cur)
+            fg.replay()
+            b_.record(cur)
+        torch.cuda.synchronize()
+        f_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in fev)
+        graph = {"value": case.ops / ((g_ms - f_ms) * 1e-3) / 1e12, "ms_per_step": g_ms - f_ms,
+                 "note": "graph replay of flush + w8a8_linear, minus the flush replayed alone"}
+        st, bits_ = w8.read_status(ws)
+        if st != 0:
+            raise RuntimeError("device status %d bits %#x after graph replays" % (st, bits_))
+    except RuntimeError:
+        raise
+    except Exception as exc:  # capture unsupported: report why
+        graph = {"value": None, "ms_per_step": None, "error": "%s: %s" % (type(exc).__name__, exc)}
+
     # End to end through the public C call with host buffers
     # (w8a8_linear_host): the copy of X in and of Y out are inside the timed
     # region, pipelined over row chunks against the compute.
@@ -464,6 +516,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
                     "d2h_bytes_per_step": Yh.numel() * Yh.element_size()},
             "gpu_launches": launches,
+            "graph": graph,
             "kernel_split_ms": {"quant": quant_ms, "gemm": gemm_ms,
                                 "note": "each kernel alone (event between them); the step overlaps the "
                                         "GEMM's set-up with the quantiser's tail"},

@@ -92,8 +92,11 @@ struct GemmCfg {
         1024 /* alignment slack */ + kStages * kStageBytes + kStagingBytes + kParamBytes + 256 /* barriers */;
 };
 static_assert(GemmCfg<1>::kSmemBytes <= 227 * 1024 && GemmCfg<2>::kSmemBytes <= 227 * 1024, "shared memory");
-static_assert((2 * GemmCfg<2>::kStages + 5) * 8 + 4 <= 256 && (2 * GemmCfg<1>::kStages + 5) * 8 + 4 <= 256,
+static_assert((2 * GemmCfg<2>::kStages + 6) * 8 + 4 <= 256 && (2 * GemmCfg<1>::kStages + 6) * 8 + 4 <= 256,
               "barrier area");
+static_assert(GemmCfg<1>::kStages * GemmCfg<1>::kStageBytes >= kPartialInt4 * 16 &&
+                  GemmCfg<2>::kStages * GemmCfg<2>::kStageBytes >= kPartialInt4 * 16,
+              "a partial tile fits in the operand ring");
 
 // Status bits (same values as W8A8_DEV_* in the public header).
 constexpr uint32_t kDevTimeoutProducer = 0x1;
@@ -193,8 +196,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = bars + 2 * S;           // [2] MMA -> epilogue
     uint64_t* tempty = tfull + 2;             // [2] epilogue -> MMA (the leader's counts both CTAs)
     uint64_t* done = tempty + 2;              // MMA teardown
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* fixbar = done + 1;              // split fix-up: partial tiles copied into the idle ring
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fixbar + 1);
     __shared__ int s_last_arrival;
+    __shared__ int s_fix_status;   // split fix-up: 1 partial copied, 2 its copy timed out
     __shared__ int s_chunk_ready[2];
 
     const int warp = threadIdx.x >> 5;
@@ -218,6 +223,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], kPair * kEpiWarps);
         }
         mbar_init(done, 1);
+        mbar_init(fixbar, 1);
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
@@ -407,6 +413,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int g = 0; g < 32; ++g)
                     __stcg(mine + (e * 32 + g) * 32 + lane,
                            make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
+                fence_proxy_async_global();   // the last segment reads the slot by bulk copy
                 __threadfence();
                 epi_barrier();
                 const int counter = (u.tile - p.dp_tiles) * kPair + static_cast<int>(rank);
@@ -416,28 +423,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 epi_barrier();
                 if (!s_last_arrival) continue;
                 __threadfence();
+                // This was the CTA's last unit, so its operand ring is idle (the
+                // MMAs that read it are complete): each other segment's partial
+                // comes in as one asynchronous bulk copy of 128 KB into the ring
+                // and is added from shared memory, instead of as rounds of
+                // dependent L2 loads.
                 const int first = (u.tile - p.dp_tiles) * p.splits;
-                for (int unit = first; unit < first + p.splits; ++unit) {
+                uint32_t fix_phase = 0;
+                bool fix_ok = true;
+                for (int unit = first; unit < first + p.splits && fix_ok; ++unit) {
                     if (unit == u.slot) continue;
-                    const int4* other = p.partials + (static_cast<int64_t>(unit) * kPair + rank) * kPartialInt4 +
-                                        e * 32 * 32 + lane;
-                    // Eight 16-byte loads in flight per batch: enough to cover
-                    // L2 latency across 256 threads, few enough registers that
-                    // the 128 running sums stay in registers.
+                    const int4* other = p.partials + (static_cast<int64_t>(unit) * kPair + rank) * kPartialInt4;
+                    if (e == 0 && lane == 0) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(fixbar, kPartialInt4 * 16);
 #pragma unroll
-                    for (int gb = 0; gb < 32; gb += 8) {
-                        int4 v[8];
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) v[g] = __ldcg(other + (gb + g) * 32);
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            acc[4 * (gb + g)] += v[g].x;
-                            acc[4 * (gb + g) + 1] += v[g].y;
-                            acc[4 * (gb + g) + 2] += v[g].z;
-                            acc[4 * (gb + g) + 3] += v[g].w;
-                        }
-                        asm volatile("" ::: "memory");   // keep the batches apart
+                        for (int c = 0; c < 8; ++c)
+                            bulk_load(smem + c * 16384, reinterpret_cast<const uint8_t*>(other) + c * 16384, 16384,
+                                      fixbar);
+                        s_fix_status = mbar_wait(fixbar, fix_phase, limit) ? 1 : 2;
                     }
+                    epi_barrier();
+                    fix_ok = (s_fix_status == 1);
+                    if (fix_ok) {
+                        const int4* sp = reinterpret_cast<const int4*>(smem) + e * 32 * 32 + lane;
+#pragma unroll
+                        for (int g = 0; g < 32; ++g) {
+                            const int4 v = sp[g * 32];
+                            acc[4 * g] += v.x;
+                            acc[4 * g + 1] += v.y;
+                            acc[4 * g + 2] += v.z;
+                            acc[4 * g + 3] += v.w;
+                        }
+                    }
+                    epi_barrier();   // everyone has read it before the next copy lands
+                    fix_phase ^= 1u;
+                }
+                if (!fix_ok) {
+                    if (e == 0 && lane == 0) atomicOr(p.status, kDevTimeoutEpilogue);
+                    ok = false;
+                    break;
                 }
                 if (e == 0 && lane == 0) p.tile_counters[counter] = 0u;   // ready for the next launch
             }

@@ -74,6 +74,15 @@ __device__ __forceinline__ void grid_wait_prerequisites()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- global visibility
+
+// Orders this thread's generic-proxy global accesses with async-proxy (TMA,
+// bulk copy) accesses of the same memory, in both directions.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
@@ -152,6 +161,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
+}
+
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) global -> shared; completion is counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
 }
 
 // As tma_load_2d, for CTA pairs: the completion is counted on the mbarrier
