@@ -100,14 +100,15 @@ def test_workspace_min_bytes(lib):
     (28672, 4096, 4096, (1776, 4, 64, 148, 2)),        # 1792 tiles, 16 left: 74 // 16 = 4
     (6144, 16384, 4096, (1536, 1, 0, 148, 2)),         # 56 left > 37: the last wave is mostly full
     (28672, 16384, 4096, (7168, 1, 0, 148, 2)),
-    (1001, 2048, 2048, (0, 2, 64, 128, 2)),            # 32 tiles on 74 pairs: cut in 2
+    (1001, 2048, 2048, (32, 1, 0, 64, 2)),             # 32 k-blocks: tiles this short are never cut
     (1001, 8192, 2048, (128, 1, 0, 148, 2)),           # 128 tiles: 54 left > 37
     (256 * 37, 512, 4096, (74, 1, 0, 148, 2)),         # exactly one wave
     # M <= 128: 128 x 256 tiles on single CTAs.
-    (126, 2048, 2048, (0, 5, 40, 40, 1)),              # 8 tiles, 32 k-blocks: sqrt caps at 5
-    (126, 8192, 2048, (0, 4, 128, 128, 1)),
-    (64, 128, 256, (0, 2, 2, 2, 1)),                   # 4 k-blocks: at least 2 per segment
-    (64, 128, 64, (1, 1, 0, 1, 1)),                    # one k-block: nothing to split
+    (126, 2048, 2048, (8, 1, 0, 8, 1)),                # 8 tiles of 32 k-blocks: too short to cut
+    (126, 8192, 2048, (32, 1, 0, 32, 1)),
+    (64, 128, 256, (1, 1, 0, 1, 1)),
+    (126, 2048, 4096, (0, 8, 64, 64, 1)),              # 64 k-blocks: cut in sqrt(64) = 8
+    (128, 256, 133136, (0, 45, 45, 45, 1)),            # 2081 k-blocks: sqrt caps at 45
 ])
 def test_gemm_plan_for_workload_shapes(lib, M, N, K, plan):
     assert w8.gemm_plan(M, N, K, num_sms=148) == plan
@@ -130,7 +131,7 @@ def test_gemm_plan_respects_workspace_room(lib):
     assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=100) == (370, 3, 42, 148, 2)
     assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=55) == (384, 1, 0, 148, 2)
     assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=0) == (384, 1, 0, 148, 2)
-    assert w8.gemm_plan(126, 2048, 2048, 148, max_slots=16) == (0, 2, 16, 16, 1)
+    assert w8.gemm_plan(126, 2048, 4096, 148, max_slots=16) == (0, 2, 16, 16, 1)
 
 
 def test_gemm_plan_invariants(lib):
@@ -152,7 +153,7 @@ def test_gemm_plan_invariants(lib):
                     else:
                         rem = tiles - dp
                         assert rem == tiles % workers and 0 < 2 * rem <= workers
-                        assert units == rem * s <= workers and kb // s >= 2
+                        assert units == rem * s <= workers and kb // s >= 2 and kb >= 48
                         assert s * s <= kb and rem * pair <= 240
                         assert grid == (workers if tiles >= workers else units) * pair
 

@@ -109,8 +109,9 @@ def test_s32_workload_codes_full(cuda_device, name):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (300, 520, 1040),        # 9 tiles on 148 SMs: every tile cut along K
-    (128 * 151, 256, 1024),  # 148 whole tiles, then 3 tiles cut in 4
+    (300, 520, 3072),        # 6 pair tiles on 74 pairs: every tile cut in 6 along K
+    (256 * 75, 256, 4096),   # 74 whole pair tiles, then 1 tile cut in 8
+    (100, 264, 4096),        # single-CTA tiles, 2 tiles cut in 8
     (128, 256, 133136),      # one tile cut into 45 segments of ~46 k-blocks
 ])
 def test_s32_k_split_and_whole_tiles_agree(cuda_device, M, N, K):

@@ -153,6 +153,11 @@ struct GemmPlan {
 };
 
 constexpr int kMinKbPerSplit = 2;
+// Tiles shorter than this many k-blocks are never split: measured on the
+// B300, the fix-up (partials written, fenced, copied back) then costs more
+// than the shorter segments save (K = 2048 shapes ran 1-2 us slower split,
+// a 256-deep tile 5 us slower; K = 4096 and 16384 ran 3 and 47 us faster).
+constexpr int64_t kMinKbToSplit = 48;
 
 // `workers`: CTAs (pair 1) or co-resident CTA pairs (pair 2).
 // `max_slots`: partial-tile slots (128 x 256 INT32 each) in the workspace.
@@ -168,7 +173,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int pair, int workers, int64
     g.tail_units = 0;
     g.grid = static_cast<int>(tiles < workers ? tiles : workers) * pair;
     const int64_t rem = tiles % workers;
-    if (rem == 0 || 2 * rem > workers || rem * pair > kMaxSplitTiles) return g;
+    if (rem == 0 || 2 * rem > workers || rem * pair > kMaxSplitTiles || num_kb < kMinKbToSplit) return g;
     int64_t s = workers / rem;
     int64_t root = 1;
     while ((root + 1) * (root + 1) <= num_kb) ++root;
