@@ -282,6 +282,36 @@ W8A8_API w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M
                                       int64_t chunk_rows, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The native BF16 linear, for the branches the guarded W8A8 path does not
+ * take.  The zhidx TurboT2VA article (section 01 item 3, "量化策略") has branches
+ * whose shapes the optimised operator cannot take fall back to native BF16,
+ * and the paperlayer summary of arXiv 2608.24674 (section "C. Fused
+ * Multimodal Transformer Operations") guards the acceleration by
+ * architectural role as well as by shape.  Same tcgen05 GEMM, with the bf16
+ * operands loaded as they are and fp32 accumulation:
+ *   Y[m][n] = bf16_rne(sum_k X[m][k] * W[n][k] + bias[n])
+ * (the products are exact in fp32; the sum is accumulated in fp32 by the
+ * tensor cores in K-chunks of 1024 and the chunks are added in fp32, so it
+ * is within fp32 rounding of the exact sum, not bit-reproducible against
+ * another summation order).
+ *   X    [M][K] bf16                                    in
+ *   W    [N][K] bf16                                    in
+ *   bias [N] of `bias_dtype` (F32 or BF16), or NULL     in
+ *   Y    [M][N] bf16                                    out
+ *   ws   >= 2048 bytes; w8a8_bf16_linear_workspace_bytes(M, N, K) for full
+ *        speed (adds the K-split partial tiles, as for w8a8_linear)
+ * Shapes: M >= 1, N >= 8 with N % 8 == 0, K >= 8 with K % 8 == 0 (16-byte
+ * rows for the tensor copies); no limit on K.  Others return
+ * W8A8_ERR_UNSUPPORTED_SHAPE with nothing launched; w8a8_bf16_linear_supported
+ * reports which (W8A8_REASON_* bits).
+ * ------------------------------------------------------------------------- */
+W8A8_API int w8a8_bf16_linear_supported(int64_t M, int64_t N, int64_t K, int bias_dtype, int* reason);
+W8A8_API size_t w8a8_bf16_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+W8A8_API w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, const uint16_t* W, int64_t N,
+                                      const void* bias, int bias_dtype, uint16_t* Y, void* ws, size_t ws_bytes,
+                                      void* stream);
+
+/* ---------------------------------------------------------------------------
  * Device status of the last call that used `ws`: synchronises `stream`,
  * copies the workspace's status word to *device_bits (host pointer) and
  * returns W8A8_OK when it is 0, W8A8_ERR_TIMEOUT when a bounded device wait

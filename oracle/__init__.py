@@ -20,6 +20,10 @@ Functions:
   epilogue(acc, sx, sw, b)  -> (y32 float32, y bf16 bits uint16)  scalar C
   bf16_rne(x float32)       -> uint16 bf16 bits                   scalar C
   linear(X, Wq, sw, bias)   -> the whole path for chosen rows
+  bf16_linear_f64(X, W, b)  -> the native BF16 linear that guard-rejected branches run:
+                               sum_k X W + b in float64 (bf16 products are exact in
+                               float64), and sum_k |X W| for the fp32-accumulation bound
+  bf16_linear_tolerance(..) -> that bound, per output
 
 bf16 tensors are passed as their raw 16-bit patterns (numpy uint16).
 """
@@ -194,3 +198,37 @@ def ulp_bf16(v: np.ndarray) -> np.ndarray:
     e = np.floor(np.log2(np.where(v > 0, v, 1.0)))
     e = np.maximum(e, -126.0)
     return np.exp2(e - 7.0)
+
+
+def bf16_linear_f64(X_bits: np.ndarray, W_bits: np.ndarray, bias=None, rows=None):
+    """The native BF16 linear (the branches the guarded W8A8 path does not
+    take fall back to it: zhidx article, section 01 item 3), exactly enough
+    to bound an fp32-accumulating GPU result.
+
+    X_bits [M, K], W_bits [N, K] are bf16 bit patterns (uint16); bias is
+    float32 [N] or None.  Every product of two bf16 values has at most 16
+    significant bits and is exact in float64; the float64 sum is within
+    K * 2^-53 * sum|x w| of the exact sum.  Returns (y64 [R, N], absum
+    [R, N]) for the chosen rows, with absum = sum_k |x_k w_k| + |bias|.
+    """
+    if rows is None:
+        rows = np.arange(X_bits.shape[0], dtype=np.int64)
+    x = bf16_bits_to_f32(np.ascontiguousarray(X_bits[rows])).astype(np.float64)
+    w = bf16_bits_to_f32(np.ascontiguousarray(W_bits)).astype(np.float64)
+    y = x @ w.T
+    absum = np.abs(x) @ np.abs(w).T
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)
+        y = y + b[None, :]
+        absum = absum + np.abs(b)[None, :]
+    return y, absum
+
+
+def bf16_linear_tolerance(y64: np.ndarray, absum: np.ndarray, K: int) -> np.ndarray:
+    """Bound on |Y - y64| for Y = bf16(fp32-accumulated sum + bias): one bf16
+    ulp of the result (final rounding, with margin) plus 2 * (K + 1) * 2^-24 *
+    sum|x w| (K + 1 fp32 additions of terms bounded by sum|x w|, each off by
+    at most one fp32 ulp of the running sum: the usual recursive-summation
+    bound, doubled for truncating adders)."""
+    return ulp_bf16(y64) + 2.0 * (K + 1) * np.exp2(-24.0) * absum
+

@@ -199,3 +199,41 @@ def test_host_pipeline_argument_errors(lib):
     assert f(p, 1, 64, 250, p, p, 128, null, 1, p, p, p, p, 1 << 20, 0, null) == 4
     assert f(p, 1, 64, 256, p, p, 128, null, 1, p, p, p, p, 64, 0, null) == 5
     assert f(p, 1, 64, 256, p, p, 128, null, 1, p, ctypes.c_void_p(0x10008), p, p, 1 << 20, 0, null) == 3
+
+
+@pytest.mark.parametrize("M,N,K,bias,ok,reasons", [
+    (1, 8, 8, w8.BF16, True, []),
+    (6144, 4096, 4096, w8.F32, True, []),
+    (64, 128, 1032, w8.BF16, True, []),          # the INT8 guard rejects K = 8 (mod 16)
+    (128, 256, 140000, w8.BF16, True, []),       # past the INT8 path's K limit
+    (0, 8, 8, w8.BF16, False, ["M"]),
+    (4, 12, 8, w8.BF16, False, ["N"]),
+    (4, 8, 20, w8.BF16, False, ["K"]),
+    (4, 8, 8, 7, False, ["BIAS_DTYPE"]),
+])
+def test_bf16_linear_guard(lib, M, N, K, bias, ok, reasons):
+    r = ctypes.c_int(0)
+    assert bool(lib.w8a8_bf16_linear_supported(M, N, K, bias, ctypes.byref(r))) == ok
+    assert [v for k, v in w8.REASONS.items() if r.value & k] == reasons
+    assert (w8.bf16_linear_workspace_bytes(M, N, K) > 0) == (ok or reasons == ["BIAS_DTYPE"])
+
+
+def test_bf16_linear_workspace_sizes(lib):
+    """Header only (2 KB with the alignment slack), plus 128 KB per CTA of
+    each K-segment when the plan cuts the last wave."""
+    assert w8.bf16_linear_workspace_bytes(1, 8, 8) == 2048
+    assert w8.bf16_linear_workspace_bytes(6144, 4096, 4096) == 2048 + 70 * 2 * SLOT   # 14 tiles x 5 segments, two CTAs each
+    assert w8.bf16_linear_workspace_bytes(64, 128, 1032) == 2048
+
+
+def test_bf16_linear_argument_errors(lib):
+    p = ctypes.c_void_p(0x10000)
+    null = None
+    f = lib.w8a8_bf16_linear
+    assert f(null, 64, 256, p, 128, null, 1, p, p, 1 << 20, null) == 1
+    assert f(p, 64, 256, p, 128, p, 9, p, p, 1 << 20, null) == 2
+    assert f(p, 64, 250, p, 128, null, 1, p, p, 1 << 20, null) == 4
+    assert f(p, 64, 256, p, 12, null, 1, p, p, 1 << 20, null) == 4
+    assert f(p, 64, 256, p, 128, null, 1, p, p, 100, null) == 5
+    assert f(p, 64, 256, p, 128, null, 1, p, null, 1 << 20, null) == 5
+    assert f(p, 64, 256, ctypes.c_void_p(0x10008), 128, null, 1, p, p, 1 << 20, null) == 3

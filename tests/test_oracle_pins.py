@@ -359,3 +359,53 @@ def test_ulp_bf16():
     assert oracle.ulp_bf16(np.array([-2.0]))[0] == 2.0 ** -6
     assert oracle.ulp_bf16(np.array([0.3]))[0] == 2.0 ** -9
     assert math.isclose(oracle.ulp_bf16(np.array([1e-39]))[0], 2.0 ** -133)
+
+
+# ---------------------------------------------------------------- native BF16 linear reference
+
+def _bf16(a):
+    """float values -> bf16 bit patterns by truncation of exactly representable values."""
+    return (np.asarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_bf16_linear_brute_force():
+    """Pure-Python triple loop on a small case (values exact in bf16)."""
+    rng = np.random.default_rng(3)
+    Xv = rng.integers(-8, 9, size=(3, 5)).astype(np.float32) / 4
+    Wv = rng.integers(-8, 9, size=(4, 5)).astype(np.float32) / 8
+    b = np.array([0.5, -1.0, 0.25, 0.0], dtype=np.float32)
+    y, absum = oracle.bf16_linear_f64(_bf16(Xv), _bf16(Wv), b)
+    for m in range(3):
+        for n in range(4):
+            want = sum(float(Xv[m, k]) * float(Wv[n, k]) for k in range(5)) + float(b[n])
+            wabs = sum(abs(float(Xv[m, k]) * float(Wv[n, k])) for k in range(5)) + abs(float(b[n]))
+            assert y[m, n] == want and absum[m, n] == wabs
+
+
+def test_bf16_linear_identity_and_roles():
+    """W = identity gives X (+ bias); a permuted identity permutes columns:
+    pins the operand roles (Y = X W^T, not W X^T)."""
+    rng = np.random.default_rng(4)
+    Xv = rng.standard_normal((6, 8)).astype(np.float32)
+    xb = _bf16(Xv)
+    x = oracle.bf16_bits_to_f32(xb).astype(np.float64)
+    eye = _bf16(np.eye(8, dtype=np.float32))
+    y, _ = oracle.bf16_linear_f64(xb, eye)
+    assert np.array_equal(y, x)
+    perm = rng.permutation(8)
+    y, _ = oracle.bf16_linear_f64(xb, eye[perm])
+    assert np.array_equal(y, x[:, perm])
+    y, _ = oracle.bf16_linear_f64(xb, eye, np.full(8, 2.0, dtype=np.float32))
+    assert np.array_equal(y, x + 2.0)
+
+
+def test_bf16_linear_closed_form_and_tolerance():
+    """All-ones rows against all-0.5 weights sum to K / 2 exactly; the bound
+    is at least one bf16 ulp and grows with K * sum|x w|."""
+    K = 4096
+    y, absum = oracle.bf16_linear_f64(_bf16(np.ones((2, K))), _bf16(np.full((3, K), 0.5)))
+    assert (y == K / 2).all() and (absum == K / 2).all()
+    tol = oracle.bf16_linear_tolerance(y, absum, K)
+    assert (tol >= oracle.ulp_bf16(y)).all()
+    assert np.allclose(tol, oracle.ulp_bf16(y) + 2 * (K + 1) * 2.0 ** -24 * absum)
+

@@ -10,7 +10,9 @@ The layer (zhidx TurboT2VA article, section 01 item 3 "量化策略"): the weigh
 is quantised once to INT8 per output channel, the activation per row on every
 call, the product accumulates in INT32, and the two scales and the bias are
 applied once after the full accumulation.  Shapes the guard rejects raise
-``UnsupportedShape``; the caller runs its BF16 linear for them.
+``UnsupportedShape`` from ``linear``; ``bf16_linear`` runs them natively on
+the same tensor-core GEMM with fp32 accumulation, and ``GuardedLinear``
+chooses between the two paths.
 """
 import ctypes
 import os
@@ -20,8 +22,9 @@ import torch
 __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
     "quantize_act", "pack_weight", "workspace_bytes", "workspace_min_bytes", "gemm_plan", "linear", "linear_quant_stage",
-    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "linear_host", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
-    "W8A8Linear", "F32", "BF16", "MAX_K",
+    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "linear_host", "bf16_linear", "bf16_linear_supported",
+    "bf16_linear_workspace_bytes", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
+    "W8A8Linear", "GuardedLinear", "F32", "BF16", "MAX_K",
 ]
 
 F32 = 0
@@ -80,6 +83,9 @@ def _load():
         "w8a8_gemm_s32": ([p, p, i64, i64, i64, p, p, sz, p], i32),
         "w8a8_linear_noalloc": ([p, i32, i64, i64, p, p, i64, p, i32, p, p], i32),
         "w8a8_linear_host": ([p, i32, i64, i64, p, p, i64, p, i32, p, p, p, p, sz, i64, p], i32),
+        "w8a8_bf16_linear_supported": ([i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)], i32),
+        "w8a8_bf16_linear_workspace_bytes": ([i64, i64, i64], sz),
+        "w8a8_bf16_linear": ([p, i64, i64, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "w8a8_debug_skip_loads": ([i32], None),
@@ -284,6 +290,45 @@ def linear_host(X_host: torch.Tensor, Wp: torch.Tensor, sw: torch.Tensor, bias=N
     return out
 
 
+def bf16_linear_supported(M: int, N: int, K: int, bias_dtype=torch.bfloat16):
+    """(supported, [reason names]) for the native BF16 linear (host only)."""
+    r = ctypes.c_int(0)
+    bd = {torch.float32: F32, torch.bfloat16: BF16}.get(bias_dtype, 99)
+    ok = _load().w8a8_bf16_linear_supported(M, N, K, bd, ctypes.byref(r))
+    return bool(ok), [v for k, v in REASONS.items() if r.value & k]
+
+
+def bf16_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_load().w8a8_bf16_linear_workspace_bytes(M, N, K))
+
+
+def bf16_linear(X: torch.Tensor, W: torch.Tensor, bias=None, out=None, workspace=None,
+                stream=None) -> torch.Tensor:
+    """The native BF16 linear on the same tcgen05 GEMM: Y = bf16(X W^T + bias)
+    with fp32 accumulation, for the layers and shapes that do not take the
+    W8A8 path (X [M, K] and W [N, K] bfloat16)."""
+    _cuda2d(X, "X")
+    _cuda2d(W, "W")
+    if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("bf16_linear takes bfloat16 X and W")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("K mismatch: X %s, W %s" % (tuple(X.shape), tuple(W.shape)))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        need = bf16_linear_workspace_bytes(M, N, K)
+        if need == 0:
+            raise UnsupportedShape(4, "bf16 linear workspace size")
+        workspace = torch.empty((need,), dtype=torch.uint8, device=X.device)
+    bdt = _dt(bias) if bias is not None else BF16
+    _check(_load().w8a8_bf16_linear(_ptr(X), M, K, _ptr(W), N, _ptr(bias), bdt, _ptr(out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "w8a8_bf16_linear")
+    return out
+
+
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -352,3 +397,36 @@ class W8A8Linear:
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty((need,), dtype=torch.uint8, device=X.device)
         return linear(X, self.Wp, self.sw, self.bias, out=out, workspace=self._ws)
+
+
+class GuardedLinear:
+    """A linear layer that takes the W8A8 path where the library's shape
+    guard accepts it and the native BF16 linear (same tensor-core GEMM, fp32
+    accumulation) where it does not: the guarded W8A8 layer of the TurboT2VA
+    pages (zhidx article, section 01 item 3; arXiv paper, appendix C).
+    The choice per layer follows from (N, K, bias dtype); per call, a row
+    count the guard rejects also takes the BF16 path."""
+
+    def __init__(self, weight: torch.Tensor, bias=None):
+        _cuda2d(weight, "weight")
+        self.out_features, self.in_features = weight.shape
+        bdt = bias.dtype if bias is not None else torch.bfloat16
+        self.int8 = shape_supported(1, self.out_features, self.in_features, torch.bfloat16, bdt)[0]
+        self.bias = bias
+        self.weight = weight if weight.dtype == torch.bfloat16 else None
+        self._w8a8 = W8A8Linear(weight, bias) if self.int8 else None
+        self._ws = None
+        if not self.int8 and self.weight is None:
+            raise TypeError("a layer the INT8 guard rejects runs the BF16 linear: pass a bfloat16 weight")
+
+    def __call__(self, X: torch.Tensor, out=None) -> torch.Tensor:
+        M = X.shape[0]
+        if self._w8a8 is not None and self._w8a8.supported(M, X.dtype):
+            return self._w8a8(X, out=out)
+        if self.weight is None:
+            raise UnsupportedShape(4, "GuardedLinear: no bfloat16 weight kept for the BF16 path")
+        need = bf16_linear_workspace_bytes(M, self.out_features, self.in_features)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=X.device)
+        return bf16_linear(X, self.weight, self.bias, out=out, workspace=self._ws)
+

@@ -98,6 +98,16 @@ static_assert(GemmCfg<1>::kStages * GemmCfg<1>::kStageBytes >= kPartialInt4 * 16
                   GemmCfg<2>::kStages * GemmCfg<2>::kStageBytes >= kPartialInt4 * 16,
               "a partial tile fits in the operand ring");
 
+// What the kernel computes after the K loop:
+//   kModeW8A8  INT8 codes in, exact INT32 sums, Y = bf16(((float)acc*sx)*sw + b)
+//   kModeS32   INT8 codes in, the exact INT32 sums themselves
+//   kModeBf16  bf16 activations and weights in (the native BF16 linear that
+//              guard-rejected shapes and BF16 layers run), fp32 sums (the
+//              tensor memory chunks added in fp32), Y = bf16(acc + b)
+constexpr int kModeW8A8 = 0;
+constexpr int kModeS32 = 1;
+constexpr int kModeBf16 = 2;
+
 // Status bits (same values as W8A8_DEV_* in the public header).
 constexpr uint32_t kDevTimeoutProducer = 0x1;
 constexpr uint32_t kDevTimeoutMma = 0x2;
@@ -106,7 +116,7 @@ constexpr uint32_t kDevTimeoutTeardown = 0x8;
 
 struct GemmParams {
     int32_t M, N, K;
-    int32_t kb_per_chunk;      // k-blocks of 64 per exact fp32 chunk, 1..16
+    int32_t kb_per_chunk;      // k-blocks of 64 per TMEM accumulation (INT8 codes: 1..16, exact)
     int32_t group_m;           // tile rasterisation: m-tiles per group
     int32_t bias_mode;         // 0 none, 1 fp32, 2 bf16
     int32_t dp_tiles;          // tiles [0, dp_tiles) are whole-tile units, round-robin over the CTAs
@@ -175,7 +185,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <bool kOutS32, int kPair>
+template <int kMode, int kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_w8a8_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                              const __grid_constant__ CUtensorMap tmap_y, const GemmParams p)
@@ -212,6 +222,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int num_kb = (p.K + kBK - 1) / kBK;
     const uint64_t limit = p.wait_limit_ns;
     constexpr uint16_t kBoth = kPair == 2 ? 0x3 : 0x1;
+    constexpr bool kOutS32 = kMode == kModeS32;
+    constexpr bool kFp32Sums = kMode == kModeBf16;   // sums held as fp32 bit patterns (zero bits = +0.0f)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -355,14 +367,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if constexpr (!kOutS32) {
                 const int i = e * 32 + lane;
                 const int n = nb * kBN + i;
-                s_sw[i] = n < p.N ? p.sw[n] : 0.0f;
+                if constexpr (kMode == kModeW8A8) s_sw[i] = n < p.N ? p.sw[n] : 0.0f;
                 if (p.bias_mode == 1)
                     s_bias[i] = n < p.N ? static_cast<const float*>(p.bias)[n] : 0.0f;
                 else if (p.bias_mode == 2)
                     s_bias[i] = n < p.N ? __uint_as_float(static_cast<uint32_t>(
                                               static_cast<const uint16_t*>(p.bias)[n]) << 16)
                                         : 0.0f;
-                if (m < p.M) sxm = p.sx[m];
+                if (kMode == kModeW8A8 && m < p.M) sxm = p.sx[m];
             }
             int32_t acc[128];
 #pragma unroll
@@ -389,7 +401,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_load_32cols(taddr + j * 32, r);
                     tmem_load_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                    for (int i = 0; i < 32; ++i) {
+                        if constexpr (kFp32Sums)
+                            acc[j * 32 + i] =
+                                __float_as_int(__fadd_rn(__int_as_float(acc[j * 32 + i]), __uint_as_float(r[i])));
+                        else
+                            acc[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -431,8 +449,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int first = (u.tile - p.dp_tiles) * p.splits;
                 uint32_t fix_phase = 0;
                 bool fix_ok = true;
+                // Integer sums may be added in any order.  Floating-point sums
+                // are added in segment order, this CTA's own from its slot as
+                // well, so the result does not depend on which segment
+                // finished last.
+                if constexpr (kFp32Sums) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) acc[i] = 0;
+                }
                 for (int unit = first; unit < first + p.splits && fix_ok; ++unit) {
-                    if (unit == u.slot) continue;
+                    if (!kFp32Sums && unit == u.slot) continue;
                     const int4* other = p.partials + (static_cast<int64_t>(unit) * kPair + rank) * kPartialInt4;
                     if (e == 0 && lane == 0) {
                         fence_proxy_async_global();
@@ -450,10 +476,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int g = 0; g < 32; ++g) {
                             const int4 v = sp[g * 32];
-                            acc[4 * g] += v.x;
-                            acc[4 * g + 1] += v.y;
-                            acc[4 * g + 2] += v.z;
-                            acc[4 * g + 3] += v.w;
+                            if constexpr (kFp32Sums) {
+                                acc[4 * g] = __float_as_int(__fadd_rn(__int_as_float(acc[4 * g]), __int_as_float(v.x)));
+                                acc[4 * g + 1] =
+                                    __float_as_int(__fadd_rn(__int_as_float(acc[4 * g + 1]), __int_as_float(v.y)));
+                                acc[4 * g + 2] =
+                                    __float_as_int(__fadd_rn(__int_as_float(acc[4 * g + 2]), __int_as_float(v.z)));
+                                acc[4 * g + 3] =
+                                    __float_as_int(__fadd_rn(__int_as_float(acc[4 * g + 3]), __int_as_float(v.w)));
+                            } else {
+                                acc[4 * g] += v.x;
+                                acc[4 * g + 1] += v.y;
+                                acc[4 * g + 2] += v.z;
+                                acc[4 * g + 3] += v.w;
+                            }
                         }
                     }
                     epi_barrier();   // everyone has read it before the next copy lands
@@ -479,18 +515,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             } else {
-                // y = bf16_rne(((float)acc * sx[m]) * sw[n] + bias[n]), eight
-                // columns at a time, packed as four bf16 pairs.
+                // y = bf16_rne(((float)acc * sx[m]) * sw[n] + bias[n]) (BF16
+                // linear: bf16_rne(acc + bias[n])), eight columns at a time,
+                // packed as four bf16 pairs.
                 const float* swc = s_sw + half * 128;
                 const float* bc = s_bias + half * 128;
                 auto dequant8 = [&](int g, uint4& out) {
-                    const float4 w0 = *reinterpret_cast<const float4*>(swc + 8 * g);
-                    const float4 w1 = *reinterpret_cast<const float4*>(swc + 8 * g + 4);
-                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                     float y[8];
+                    if constexpr (kFp32Sums) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * g + i]), sxm), wv[i]);
+                        for (int i = 0; i < 8; ++i) y[i] = __int_as_float(acc[8 * g + i]);
+                    } else {
+                        const float4 w0 = *reinterpret_cast<const float4*>(swc + 8 * g);
+                        const float4 w1 = *reinterpret_cast<const float4*>(swc + 8 * g + 4);
+                        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * g + i]), sxm), wv[i]);
+                    }
                     if (p.bias_mode != 0) {
                         const float4 b0 = *reinterpret_cast<const float4*>(bc + 8 * g);
                         const float4 b1 = *reinterpret_cast<const float4*>(bc + 8 * g + 4);

@@ -124,6 +124,26 @@ bool ws_layout(int64_t M, int64_t K, WsLayout* L)
     return true;
 }
 
+// Workspace of the BF16 linear: the 1 KB header (status word and split-tile
+// counters) and the partial-tile slots; no codes, no scales.
+void bf16_ws_layout(WsLayout* L)
+{
+    L->status_off = 0;
+    L->sx_off = L->codes_off = 0;   // unused
+    L->slots_off = kAlign;
+    L->min_total = kAlign + L->slots_off;
+}
+
+int bf16_guard_reasons(int64_t M, int64_t N, int64_t K, int bias_dtype)
+{
+    int r = 0;
+    if (M < 1 || M > INT32_MAX) r |= W8A8_REASON_M;
+    if (N < 8 || N % 8 != 0 || N > INT32_MAX) r |= W8A8_REASON_N;
+    if (K < 8 || K % 8 != 0 || K > INT32_MAX) r |= W8A8_REASON_K;
+    if (bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) r |= W8A8_REASON_BIAS_DTYPE;
+    return r;
+}
+
 // Partial-tile slots that fit in a workspace of ws_bytes.
 int64_t ws_slots(const WsLayout& L, size_t ws_bytes)
 {
@@ -197,10 +217,10 @@ GemmPlan choose_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_work
     return plan_gemm(M, N, K, 1, num_sms, max_slots);
 }
 
-template <bool kOutS32, int kPair>
+template <int kMode, int kPair>
 cudaError_t set_gemm_smem()
 {
-    return cudaFuncSetAttribute(w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, kPair>,
+    return cudaFuncSetAttribute(w8a8::gemm_w8a8_tcgen05_kernel<kMode, kPair>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(w8a8::GemmCfg<kPair>::kSmemBytes));
 }
@@ -211,8 +231,10 @@ bool ensure_gemm_ready(DeviceInfo* dev)
 {
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     if (dev->gemm_attr_set) return true;
-    if (set_gemm_smem<false, 1>() != cudaSuccess || set_gemm_smem<true, 1>() != cudaSuccess ||
-        set_gemm_smem<false, 2>() != cudaSuccess || set_gemm_smem<true, 2>() != cudaSuccess) {
+    using namespace w8a8;
+    if (set_gemm_smem<kModeW8A8, 1>() != cudaSuccess || set_gemm_smem<kModeS32, 1>() != cudaSuccess ||
+        set_gemm_smem<kModeBf16, 1>() != cudaSuccess || set_gemm_smem<kModeW8A8, 2>() != cudaSuccess ||
+        set_gemm_smem<kModeS32, 2>() != cudaSuccess || set_gemm_smem<kModeBf16, 2>() != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -228,7 +250,8 @@ bool ensure_gemm_ready(DeviceInfo* dev)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, w8a8::gemm_w8a8_tcgen05_kernel<false, 2>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&clusters, w8a8::gemm_w8a8_tcgen05_kernel<w8a8::kModeW8A8, 2>, &cfg) !=
+        cudaSuccess)
         clusters = 0;
     cudaGetLastError();
     dev->pair_workers = clusters > dev->num_sms / 2 ? dev->num_sms / 2 : clusters;
@@ -347,7 +370,7 @@ w8a8_status launch_codes_to_bf16(const int8_t* Qi, uint16_t* Qb, int64_t n, uint
 
 // ---------------------------------------------------------------- GEMM
 
-template <bool kOutS32>
+template <int kMode>
 w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t* Wp, int64_t M, int64_t N,
                         int64_t K, const float* sx, const float* sw, const void* bias, int bias_mode, void* out,
                         uint8_t* ws_aligned, const WsLayout& L, int64_t slots, cudaStream_t stream)
@@ -358,7 +381,7 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     if (!encode_bf16_2d(&ta, A_codes, M, K, w8a8::kBM)) return W8A8_ERR_CUDA;
     if (!encode_bf16_2d(&tb, Wp, N, K, static_cast<uint32_t>(w8a8::kBN / g.pair))) return W8A8_ERR_CUDA;
     // The pair form stores bf16 Y through TMA in 32-row x 64-column boxes.
-    if (!kOutS32 && g.pair == 2) {
+    if (kMode != w8a8::kModeS32 && g.pair == 2) {
         if (!encode_bf16_2d(&ty, out, M, N, 32)) return W8A8_ERR_CUDA;
     } else {
         ty = tb;   // not read by these forms
@@ -367,7 +390,10 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
-    p.kb_per_chunk = w8a8::kMaxKbPerChunk;
+    // INT8 codes: fp32 chunks short enough to be exact integers.  BF16: one
+    // fp32 accumulation over the unit's whole K range.
+    p.kb_per_chunk = kMode == w8a8::kModeBf16 ? static_cast<int32_t>((K + w8a8::kBK - 1) / w8a8::kBK)
+                                              : w8a8::kMaxKbPerChunk;
     p.group_m = 8;
     p.bias_mode = bias_mode;
     p.sx = sx;
@@ -402,11 +428,11 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     if (g.pair == 1) {
         cfg.dynamicSmemBytes = w8a8::GemmCfg<1>::kSmemBytes;
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 1>, ta, tb, ty, p);
+        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kMode, 1>, ta, tb, ty, p);
     } else {
         cfg.dynamicSmemBytes = w8a8::GemmCfg<2>::kSmemBytes;
         cfg.numAttrs = 2;
-        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kOutS32, 2>, ta, tb, ty, p);
+        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_w8a8_tcgen05_kernel<kMode, 2>, ta, tb, ty, p);
     }
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -574,7 +600,7 @@ w8a8_status w8a8_linear_gemm_stage(int64_t M, int64_t K, const uint16_t* Wp, con
     if (!dev) return W8A8_ERR_NO_DEVICE;
     uint8_t* w = ws_base(ws);
     const int bias_mode = bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0;
-    return launch_gemm<false>(dev, reinterpret_cast<const uint16_t*>(w + L.codes_off), Wp, M, N, K,
+    return launch_gemm<w8a8::kModeW8A8>(dev, reinterpret_cast<const uint16_t*>(w + L.codes_off), Wp, M, N, K,
                               reinterpret_cast<const float*>(w + L.sx_off), sw, bias, bias_mode, Y, w, L,
                               ws_slots(L, ws_bytes), static_cast<cudaStream_t>(stream));
 }
@@ -616,7 +642,8 @@ w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64
     uint16_t* codes = reinterpret_cast<uint16_t*>(w + L.codes_off);
     w8a8_status st = launch_codes_to_bf16(Xq, codes, M * K, status, dev->num_sms, s);
     if (st != W8A8_OK) return st;
-    return launch_gemm<true>(dev, codes, Wp, M, N, K, nullptr, nullptr, nullptr, 0, acc, w, L, ws_slots(L, ws_bytes),
+    return launch_gemm<w8a8::kModeS32>(dev, codes, Wp, M, N, K, nullptr, nullptr, nullptr, 0, acc, w, L,
+                                       ws_slots(L, ws_bytes),
                              s);
 }
 
@@ -712,6 +739,48 @@ w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t
         return W8A8_ERR_CUDA;
     }
     return W8A8_OK;
+}
+
+size_t w8a8_bf16_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (bf16_guard_reasons(M, N, K, W8A8_BF16) != 0) return 0;
+    WsLayout L;
+    bf16_ws_layout(&L);
+    const GemmPlan g = current_plan(M, N, K, INT64_MAX);
+    return L.min_total + static_cast<size_t>(g.tail_units * g.pair) * kSlotBytes;
+}
+
+int w8a8_bf16_linear_supported(int64_t M, int64_t N, int64_t K, int bias_dtype, int* reason)
+{
+    const int r = bf16_guard_reasons(M, N, K, bias_dtype);
+    if (reason) *reason = r;
+    return r == 0 ? 1 : 0;
+}
+
+w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, const uint16_t* W, int64_t N,
+                             const void* bias, int bias_dtype, uint16_t* Y, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!X || !W || !Y || M < 0 || N < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (bias && bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (bf16_guard_reasons(M, N, K, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    WsLayout L;
+    bf16_ws_layout(&L);
+    if (!ws || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(ws, 16)) return W8A8_ERR_ALIGNMENT;
+    if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
+    int devno = 0;
+    DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(&devno));
+    if (!dev) return W8A8_ERR_NO_DEVICE;
+    uint8_t* w = ws_base(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // No quantiser runs first to clear the header: clear it here.
+    if (cudaMemsetAsync(w + L.status_off, 0, kAlign, s) != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    const int bias_mode = bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0;
+    return launch_gemm<w8a8::kModeBf16>(dev, X, W, M, N, K, nullptr, nullptr, bias, bias_mode, Y, w, L,
+                                        ws_slots(L, ws_bytes), s);
 }
 
 w8a8_status w8a8_read_status(const void* ws, void* stream, uint32_t* device_bits)
