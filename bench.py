@@ -47,7 +47,7 @@ FLUSH_BYTES = 256 << 20
 # them, and the bench reports null traffic when the sources have changed since.
 GEMM_SOURCES = ["w8a8_int8_linear_act_b300/csrc/gemm_tcgen05.cuh",
                 "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh"]
-GEMM_TRAFFIC = {"f79cb5e97886410c": 169.38e6}
+GEMM_TRAFFIC = {"87fb347344a746fa": 169.65e6}
 
 
 def sources_digest(paths):
@@ -489,6 +489,33 @@ def run_ours(args):
                 "note": "the guard's native BF16 fallback on this shape, header clear + GEMM, L2 flushed"}
         del Xb, Wb, bb, wsb
 
+    # SageSLA's per-block INT8 Query/Key quantisation at the video branch's
+    # attention shape (32 heads of 128 over this workload's tokens), each call
+    # timed alone after a flush.
+    qk = None
+    if M >= 1024:
+        heads, dh = 32, 128
+        Xqk = torch.randn((1, heads, M, dh), generator=torch.Generator().manual_seed(77)).to(torch.bfloat16).to(dev)
+        qk = {"shape": [1, heads, M, dh], "layout": "HND", "unit": "GB/s", "peak": peaks()["hbm_gbs"]}
+        for name, bt in (("query", 128), ("key", 64)):
+            for _ in range(3):
+                flush.zero_()
+                w8.quantize_qk_blocks(Xqk, bt, stream=stream)
+            qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(min(args.steps, 200))]
+            for a, b_ in qev:
+                flush.zero_()
+                a.record(stream)
+                w8.quantize_qk_blocks(Xqk, bt, stream=stream)
+                b_.record(stream)
+            torch.cuda.synchronize()
+            q_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in qev)
+            nbytes = Xqk.numel() * 3 + heads * (-(-M // bt)) * 4   # bf16 in, int8 out, one scale per block
+            gbs = nbytes / (q_ms * 1e-3) / 1e9
+            qk[name] = {"block_tokens": bt, "ms": q_ms, "achieved": gbs, "frac": gbs / qk["peak"],
+                        "algorithmic_bytes": nbytes}
+        del Xqk
+
     # End to end through the public C call with host buffers
     # (w8a8_linear_host): the copy of X in and of Y out are inside the timed
     # region, pipelined over row chunks against the compute.
@@ -551,6 +578,7 @@ def run_ours(args):
                                 "note": "each kernel alone (event between them); the step overlaps the "
                                         "GEMM's set-up with the quantiser's tail"},
             "bf16_fallback": bf16,
+            "qk_block_quant": qk,
             "clocks": clocks,
             "wall_s_timed": t_wall,
         }

@@ -312,6 +312,30 @@ W8A8_API w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, c
                                       void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Per-block INT8 quantisation of attention Query or Key (zhidx TurboT2VA
+ * article, section 01 item 4: the SageSLA self-attention path quantises
+ * Query and Key to INT8).  A block is `block_tokens` consecutive tokens of
+ * one (batch, head), the last block of a head possibly shorter; each block
+ * gets one scale and the linear layer's row rule:
+ *   s = fp32(absmax / 127) (zero block: 1), q = clamp(rne(fp32(x / s)), +-127).
+ *   X      [B][H][L][D] (layout W8A8_LAYOUT_HND) or [B][L][H][D]
+ *          (W8A8_LAYOUT_NHD) of `x_dtype` (F32 or BF16), D contiguous   in
+ *   Xq     int8 codes, same shape and layout as X                       out
+ *   scales [B][H][ceil(L / block_tokens)] fp32                         out
+ * Needs D % 8 == 0 and D <= 2048 for BF16 (D % 4 == 0 and D <= 1024 for
+ * F32), block_tokens >= 1; X and Xq 16-byte aligned.  Any of B, H, L == 0
+ * is a no-op returning W8A8_OK.  Errors: W8A8_ERR_INVALID_ARG (NULL
+ * pointer, negative size, unknown layout), W8A8_ERR_DTYPE,
+ * W8A8_ERR_UNSUPPORTED_SHAPE (D or block_tokens), W8A8_ERR_ALIGNMENT; nothing
+ * is launched on an error.  Asynchronous on `stream`.
+ * ------------------------------------------------------------------------- */
+#define W8A8_LAYOUT_HND 0
+#define W8A8_LAYOUT_NHD 1
+W8A8_API w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64_t H, int64_t L, int64_t D,
+                                             int layout, int64_t block_tokens, int8_t* Xq, float* scales,
+                                             void* stream);
+
+/* ---------------------------------------------------------------------------
  * Device status of the last call that used `ws`: synchronises `stream`,
  * copies the workspace's status word to *device_bits (host pointer) and
  * returns W8A8_OK when it is 0, W8A8_ERR_TIMEOUT when a bounded device wait

@@ -24,6 +24,10 @@ Functions:
                                sum_k X W + b in float64 (bf16 products are exact in
                                float64), and sum_k |X W| for the fp32-accumulation bound
   bf16_linear_tolerance(..) -> that bound, per output
+  quantize_qk_blocks(X, bt, layout)
+                            -> per-block INT8 codes and scales of attention Query/Key:
+                               quantize_rows applied to each block of bt tokens of one
+                               (batch, head), flattened
 
 bf16 tensors are passed as their raw 16-bit patterns (numpy uint16).
 """
@@ -231,4 +235,28 @@ def bf16_linear_tolerance(y64: np.ndarray, absum: np.ndarray, K: int) -> np.ndar
     at most one fp32 ulp of the running sum: the usual recursive-summation
     bound, doubled for truncating adders)."""
     return ulp_bf16(y64) + 2.0 * (K + 1) * np.exp2(-24.0) * absum
+
+
+def quantize_qk_blocks(X: np.ndarray, block_tokens: int, layout: str = "HND"):
+    """Per-block INT8 quantisation of attention Query or Key (zhidx TurboT2VA
+    article, section 01 item 4: SageSLA quantises Query and Key to INT8).
+
+    X is [B, H, L, D] ("HND") or [B, L, H, D] ("NHD"), float32 or bf16 bits.
+    Each block of ``block_tokens`` consecutive tokens of one (batch, head),
+    the last one possibly shorter, is flattened to one row and quantised by
+    ``quantize_rows`` (one scale per block).  Returns (codes int8 in X's
+    shape, scales float32 [B, H, nblk])."""
+    Xh = X if layout == "HND" else X.transpose(0, 2, 1, 3)
+    B, H, L, D = Xh.shape
+    bt = min(block_tokens, L)
+    nblk = -(-L // bt)
+    q = np.empty((B, H, L, D), dtype=np.int8)
+    s = np.empty((B, H, nblk), dtype=np.float32)
+    for j in range(nblk):
+        t0, t1 = j * bt, min(L, (j + 1) * bt)
+        rows = np.ascontiguousarray(Xh[:, :, t0:t1, :]).reshape(B * H, (t1 - t0) * D)
+        qj, sj = quantize_rows(rows)
+        q[:, :, t0:t1, :] = qj.reshape(B, H, t1 - t0, D)
+        s[:, :, j] = sj.reshape(B, H)
+    return (q if layout == "HND" else np.ascontiguousarray(q.transpose(0, 2, 1, 3))), s
 

@@ -237,3 +237,18 @@ def test_bf16_linear_argument_errors(lib):
     assert f(p, 64, 256, p, 128, null, 1, p, p, 100, null) == 5
     assert f(p, 64, 256, p, 128, null, 1, p, null, 1 << 20, null) == 5
     assert f(p, 64, 256, ctypes.c_void_p(0x10008), 128, null, 1, p, p, 1 << 20, null) == 3
+
+
+def test_qk_blocks_argument_errors(lib):
+    p = ctypes.c_void_p(0x10000)
+    null = None
+    f = lib.w8a8_quantize_qk_blocks
+    assert f(p, w8.BF16, 1, 2, 0, 64, 0, 64, null, null, null) == 0     # empty: no-op
+    assert f(null, w8.BF16, 1, 2, 8, 64, 0, 64, p, p, null) == 1
+    assert f(p, w8.BF16, 1, 2, 8, 64, 2, 64, p, p, null) == 1          # unknown layout
+    assert f(p, 5, 1, 2, 8, 64, 0, 64, p, p, null) == 2
+    assert f(p, w8.BF16, 1, 2, 8, 60, 0, 64, p, p, null) == 4          # D % 8
+    assert f(p, w8.BF16, 1, 2, 8, 4096, 0, 64, p, p, null) == 4        # D > 2048
+    assert f(p, w8.F32, 1, 2, 8, 2048, 0, 64, p, p, null) == 4         # fp32 D > 1024
+    assert f(p, w8.BF16, 1, 2, 8, 64, 0, 0, p, p, null) == 4           # block_tokens 0
+    assert f(ctypes.c_void_p(0x10008), w8.BF16, 1, 2, 8, 64, 0, 64, p, p, null) == 3

@@ -409,3 +409,74 @@ def test_bf16_linear_closed_form_and_tolerance():
     assert (tol >= oracle.ulp_bf16(y)).all()
     assert np.allclose(tol, oracle.ulp_bf16(y) + 2 * (K + 1) * 2.0 ** -24 * absum)
 
+
+
+# ---------------------------------------------------------------- per-block Query/Key quantisation
+
+def _py_block_quant(vals):
+    """Pure-Python restatement on one block: fp32 absmax / 127, then each
+    code round-half-even of the fp32 quotient, clamped."""
+    f32 = np.float32
+    amax = max(abs(float(v)) for v in vals)
+    s = f32(f32(amax) / f32(127.0))
+    if s == 0:
+        return [0] * len(vals), f32(1.0)
+    codes = [max(-127, min(127, round(float(f32(f32(v) / s))))) for v in vals]
+    return codes, s
+
+
+def test_qk_blocks_brute_force():
+    rng = np.random.default_rng(21)
+    X = rng.standard_normal((2, 3, 5, 4)).astype(np.float32)
+    X[1, 2, 2:4] = 0.0                                  # one all-zero block
+    q, s = oracle.quantize_qk_blocks(X, 2, "HND")
+    assert q.shape == X.shape and s.shape == (2, 3, 3)
+    for b in range(2):
+        for h in range(3):
+            for j, (t0, t1) in enumerate([(0, 2), (2, 4), (4, 5)]):
+                codes, sc = _py_block_quant(X[b, h, t0:t1].ravel())
+                assert s[b, h, j] == sc
+                assert list(q[b, h, t0:t1].ravel()) == codes
+    assert s[1, 2, 1] == 1.0 and not q[1, 2, 2:4].any()
+
+
+def test_qk_blocks_layouts_agree():
+    """NHD input is the HND tensor with heads and tokens swapped: the codes
+    swap the same way and the scales are identical."""
+    rng = np.random.default_rng(22)
+    X = rng.standard_normal((2, 4, 37, 16)).astype(np.float32)
+    qh, sh = oracle.quantize_qk_blocks(X, 8, "HND")
+    qn, sn = oracle.quantize_qk_blocks(np.ascontiguousarray(X.transpose(0, 2, 1, 3)), 8, "NHD")
+    assert np.array_equal(sh, sn)
+    assert np.array_equal(qn, qh.transpose(0, 2, 1, 3))
+
+
+def test_qk_blocks_special_block_sizes():
+    """One token per block is per-token quantisation; one block per head is
+    the head flattened to one row."""
+    rng = np.random.default_rng(23)
+    X = (rng.standard_normal((1, 3, 10, 8)) * 3).astype(np.float32)
+    q1, s1 = oracle.quantize_qk_blocks(X, 1)
+    qr, sr = oracle.quantize_rows(X.reshape(30, 8))
+    assert np.array_equal(q1.reshape(30, 8), qr) and np.array_equal(s1.reshape(30), sr)
+    qa, sa = oracle.quantize_qk_blocks(X, 1000)
+    qr, sr = oracle.quantize_rows(X.reshape(3, 80))
+    assert np.array_equal(qa.reshape(3, 80), qr) and np.array_equal(sa.reshape(3), sr)
+
+
+def test_qk_blocks_are_independent_and_saturate():
+    """Scaling one block by 2^3 scales only its scale (codes unchanged), and
+    every nonzero block reaches |q| = 127."""
+    rng = np.random.default_rng(24)
+    X = rng.standard_normal((1, 2, 12, 8)).astype(np.float32)
+    q, s = oracle.quantize_qk_blocks(X, 4)
+    Y = X.copy()
+    Y[0, 1, 4:8] *= 8.0
+    q2, s2 = oracle.quantize_qk_blocks(Y, 4)
+    assert np.array_equal(q2, q)
+    assert s2[0, 1, 1] == 8 * s[0, 1, 1]
+    s2[0, 1, 1] = s[0, 1, 1]
+    assert np.array_equal(s2, s)
+    for h in range(2):
+        for j in range(3):
+            assert np.abs(q[0, h, 4 * j:4 * j + 4].astype(np.int32)).max() == 127

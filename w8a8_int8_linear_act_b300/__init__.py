@@ -23,7 +23,7 @@ __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
     "quantize_act", "pack_weight", "workspace_bytes", "workspace_min_bytes", "gemm_plan", "linear", "linear_quant_stage",
     "linear_gemm_stage", "gemm_s32", "linear_noalloc", "linear_host", "bf16_linear", "bf16_linear_supported",
-    "bf16_linear_workspace_bytes", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
+    "bf16_linear_workspace_bytes", "quantize_qk_blocks", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
     "W8A8Linear", "GuardedLinear", "F32", "BF16", "MAX_K",
 ]
 
@@ -86,6 +86,7 @@ def _load():
         "w8a8_bf16_linear_supported": ([i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)], i32),
         "w8a8_bf16_linear_workspace_bytes": ([i64, i64, i64], sz),
         "w8a8_bf16_linear": ([p, i64, i64, p, i64, p, i32, p, p, sz, p], i32),
+        "w8a8_quantize_qk_blocks": ([p, i32, i64, i64, i64, i64, i32, i64, p, p, p], i32),
         "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "w8a8_debug_skip_loads": ([i32], None),
@@ -327,6 +328,32 @@ def bf16_linear(X: torch.Tensor, W: torch.Tensor, bias=None, out=None, workspace
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "w8a8_bf16_linear")
     return out
+
+
+LAYOUTS = {"HND": 0, "NHD": 1}
+
+
+def quantize_qk_blocks(X: torch.Tensor, block_tokens: int, layout: str = "HND", stream=None):
+    """Per-block INT8 quantisation of attention Query or Key (the SageSLA
+    path's INT8 Q/K).  X is [B, H, L, D] ("HND") or [B, L, H, D] ("NHD"),
+    contiguous.  Returns (codes int8, same shape; scales float32
+    [B, H, ceil(L / block_tokens)])."""
+    if not X.is_cuda or X.dim() != 4 or not X.is_contiguous():
+        raise ValueError("X must be a contiguous 4-D CUDA tensor")
+    if layout not in LAYOUTS:
+        raise ValueError("layout must be 'HND' or 'NHD'")
+    if layout == "HND":
+        B, H, L, D = X.shape
+    else:
+        B, L, H, D = X.shape
+    if block_tokens < 1:
+        raise ValueError("block_tokens must be >= 1")
+    nblk = -(-L // block_tokens) if L > 0 else 0
+    Xq = torch.empty(X.shape, dtype=torch.int8, device=X.device)
+    S = torch.empty((B, H, nblk), dtype=torch.float32, device=X.device)
+    _check(_load().w8a8_quantize_qk_blocks(_ptr(X), _dt(X), B, H, L, D, LAYOUTS[layout], block_tokens, _ptr(Xq),
+                                           _ptr(S), _stream(stream)), "w8a8_quantize_qk_blocks")
+    return Xq, S
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

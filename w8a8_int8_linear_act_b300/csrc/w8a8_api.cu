@@ -13,6 +13,7 @@
 #include "../../include/w8a8.h"
 #include "gemm_tcgen05.cuh"
 #include "quant_rows.cuh"
+#include "quant_blocks.cuh"
 
 namespace {
 
@@ -484,6 +485,37 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[W8A8_NOALLOC_SCRATCH_
 void* g_noalloc_ptr[kMaxDevices] = {};
 std::mutex g_noalloc_mutex;
 
+// ---------------------------------------------------------------- Query/Key blocks
+
+template <typename TIn, int NV>
+void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
+                       cudaStream_t stream)
+{
+    const unsigned threads = static_cast<unsigned>((g.tpp * g.vd + 31) / 32 * 32);
+    w8a8::quant_blocks_kernel<TIn, NV><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(X, g, Q, S);
+}
+
+template <typename TIn>
+w8a8_status launch_blocks_typed(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
+                                cudaStream_t stream)
+{
+    // Vectors one thread holds: ceil(block_tokens / tpp).
+    const int64_t per = (g.block_tokens + g.tpp - 1) / g.tpp;
+    if (per <= 1)
+        launch_blocks_cfg<TIn, 1>(X, g, blocks, Q, S, stream);
+    else if (per <= 2)
+        launch_blocks_cfg<TIn, 2>(X, g, blocks, Q, S, stream);
+    else if (per <= 4)
+        launch_blocks_cfg<TIn, 4>(X, g, blocks, Q, S, stream);
+    else if (per <= 8)
+        launch_blocks_cfg<TIn, 8>(X, g, blocks, Q, S, stream);
+    else if (per <= 16)
+        launch_blocks_cfg<TIn, 16>(X, g, blocks, Q, S, stream);
+    else
+        launch_blocks_cfg<TIn, 0>(X, g, blocks, Q, S, stream);
+    return last_launch_status();
+}
+
 }  // namespace
 
 extern "C" {
@@ -781,6 +813,49 @@ w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, const uint
     const int bias_mode = bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0;
     return launch_gemm<w8a8::kModeBf16>(dev, X, W, M, N, K, nullptr, nullptr, bias, bias_mode, Y, w, L,
                                         ws_slots(L, ws_bytes), s);
+}
+
+w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64_t H, int64_t L, int64_t D,
+                                    int layout, int64_t block_tokens, int8_t* Xq, float* scales, void* stream)
+{
+    if (B < 0 || H < 0 || L < 0 || D < 0 || block_tokens < 0) return W8A8_ERR_INVALID_ARG;
+    if (layout != W8A8_LAYOUT_HND && layout != W8A8_LAYOUT_NHD) return W8A8_ERR_INVALID_ARG;
+    if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (B == 0 || H == 0 || L == 0) return W8A8_OK;
+    if (!X || !Xq || !scales) return W8A8_ERR_INVALID_ARG;
+    const int64_t E = x_dtype == W8A8_BF16 ? 8 : 4;
+    if (D < E || D % E != 0 || D / E > 256 || block_tokens < 1) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(X, 16) || !aligned(Xq, 16) || !aligned(scales, 4)) return W8A8_ERR_ALIGNMENT;
+    w8a8::BlockGeom g;
+    g.H = H;
+    g.L = L;
+    g.block_tokens = block_tokens < L ? block_tokens : L;
+    g.nblk = (L + g.block_tokens - 1) / g.block_tokens;
+    g.vd = static_cast<int32_t>(D / E);
+    // Tokens per pass: as many as 256 threads cover (more warps per SM; a
+    // form with up to 16 vectors per thread and fewer threads measured
+    // slower at the video attention shape).
+    const int64_t cap = 256 / g.vd;
+    g.tpp = static_cast<int32_t>(cap < g.block_tokens ? cap : g.block_tokens);
+    if (layout == W8A8_LAYOUT_HND) {
+        g.stride_t = D;
+        g.stride_h = L * D;
+        g.stride_b = H * L * D;
+    } else {
+        g.stride_t = H * D;
+        g.stride_h = D;
+        g.stride_b = L * H * D;
+    }
+    // The scales follow (b, h, j) for the caller's nblk = ceil(L / block_tokens)
+    // also when block_tokens > L (then one block per head).
+    const int64_t blocks = B * H * g.nblk;
+    if (blocks > INT32_MAX) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    const DeviceInfo* dev = device_info(nullptr);
+    if (!dev) return W8A8_ERR_NO_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (x_dtype == W8A8_BF16)
+        return launch_blocks_typed<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(X), g, blocks, Xq, scales, s);
+    return launch_blocks_typed<float>(static_cast<const float*>(X), g, blocks, Xq, scales, s);
 }
 
 w8a8_status w8a8_read_status(const void* ws, void* stream, uint32_t* device_bits)
