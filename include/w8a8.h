@@ -312,6 +312,36 @@ W8A8_API w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, c
                                       void* stream);
 
 /* ---------------------------------------------------------------------------
+ * MLP pair: Y = down(up(X)), both layers on the W8A8 path, with the down
+ * layer's per-row activation quantisation fed by the up layer's epilogue.
+ * Each layer is the linear above (zhidx TurboT2VA article, section 01 item
+ * 3); between them nothing is applied (no activation function: the pages
+ * name none).  The up GEMM's epilogue gathers each row's max |H| over the
+ * bf16 values it writes (an exact integer max on the bit patterns, by
+ * atomicMax), so the down layer's codes come from one streaming pass over
+ * H with no reduction.  H, the codes and the scales are bit-identical to
+ * w8a8_linear(X) followed by w8a8_linear(H).
+ *   X      [M][K] F32 or BF16                           in
+ *   Wp_up  [F][K] packed codes, sw_up [F], bias_up [F]  in (bias nullable)
+ *   Wp_down[N][F] packed codes, sw_down [N], bias_down [N]  in
+ *   H      [M][F] bf16, the up layer's output           out
+ *   Y      [M][N] bf16                                  out
+ *   ws     >= w8a8_mlp_workspace_bytes(M, K, F, N) for full speed (the
+ *          smallest accepted holds both layers' codes and scales and no
+ *          split-tile slots); caller-owned, 16-byte aligned.
+ * Both (M, F, K) and (M, N, F) must pass w8a8_shape_supported; errors as for
+ * w8a8_linear, nothing launched on an error.  Four launches on `stream`:
+ * quantiser, up GEMM, codes pass, down GEMM, each after the first a
+ * programmatic dependent of the one before.
+ * ------------------------------------------------------------------------- */
+W8A8_API size_t w8a8_mlp_workspace_bytes(int64_t M, int64_t K, int64_t F, int64_t N);
+W8A8_API w8a8_status w8a8_mlp(const void* X, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp_up,
+                              const float* sw_up, int64_t F, const void* bias_up, int bias_up_dtype,
+                              const uint16_t* Wp_down, const float* sw_down, int64_t N, const void* bias_down,
+                              int bias_down_dtype, uint16_t* H, uint16_t* Y, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------
  * Per-block INT8 quantisation of attention Query or Key (zhidx TurboT2VA
  * article, section 01 item 4: the SageSLA self-attention path quantises
  * Query and Key to INT8).  A block is `block_tokens` consecutive tokens of

@@ -252,3 +252,29 @@ def test_qk_blocks_argument_errors(lib):
     assert f(p, w8.F32, 1, 2, 8, 2048, 0, 64, p, p, null) == 4         # fp32 D > 1024
     assert f(p, w8.BF16, 1, 2, 8, 64, 0, 0, p, p, null) == 4           # block_tokens 0
     assert f(ctypes.c_void_p(0x10008), w8.BF16, 1, 2, 8, 64, 0, 64, p, p, null) == 3
+
+
+def test_mlp_workspace_and_argument_errors(lib):
+    # both layers' activation codes and scales, the row maxima, and the slots
+    # of whichever GEMM plan wants more
+    M, K, F, N = 6144, 4096, 16384, 4096
+    base = w8.workspace_min_bytes(M, K) + 2 * 24576 + M * F * 2
+    up = w8.gemm_plan(M, F, K, num_sms=148)
+    dn = w8.gemm_plan(M, N, F, num_sms=148)
+    assert w8.mlp_workspace_bytes(M, K, F, N) == base + max(up[2] * up[4], dn[2] * dn[4]) * SLOT
+    assert w8.mlp_workspace_bytes(M, K, 1000, N) == 0          # F % 16
+    p = ctypes.c_void_p(0x10000)
+    null = None
+    f = lib.w8a8_mlp
+    args = [p, w8.BF16, 64, 256, p, p, 512, null, 1, p, p, 128, null, 1, p, p, p, 1 << 26, null]
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a14=null) == 1                                  # no H
+    assert call(a1=7) == 2
+    assert call(a6=520) == 4                                    # F % 16 (down layer's K)
+    assert call(a11=12) == 4
+    assert call(a17=64) == 5
+    assert call(a15=ctypes.c_void_p(0x10008)) == 3

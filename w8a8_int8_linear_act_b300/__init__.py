@@ -23,7 +23,7 @@ __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
     "quantize_act", "pack_weight", "workspace_bytes", "workspace_min_bytes", "gemm_plan", "linear", "linear_quant_stage",
     "linear_gemm_stage", "gemm_s32", "linear_noalloc", "linear_host", "bf16_linear", "bf16_linear_supported",
-    "bf16_linear_workspace_bytes", "quantize_qk_blocks", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
+    "bf16_linear_workspace_bytes", "quantize_qk_blocks", "mlp", "mlp_workspace_bytes", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
     "W8A8Linear", "GuardedLinear", "F32", "BF16", "MAX_K",
 ]
 
@@ -87,6 +87,8 @@ def _load():
         "w8a8_bf16_linear_workspace_bytes": ([i64, i64, i64], sz),
         "w8a8_bf16_linear": ([p, i64, i64, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_quantize_qk_blocks": ([p, i32, i64, i64, i64, i64, i32, i64, p, p, p], i32),
+        "w8a8_mlp_workspace_bytes": ([i64, i64, i64, i64], sz),
+        "w8a8_mlp": ([p, i32, i64, i64, p, p, i64, p, i32, p, p, i64, p, i32, p, p, p, sz, p], i32),
         "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "w8a8_debug_skip_loads": ([i32], None),
@@ -328,6 +330,38 @@ def bf16_linear(X: torch.Tensor, W: torch.Tensor, bias=None, out=None, workspace
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "w8a8_bf16_linear")
     return out
+
+
+def mlp_workspace_bytes(M: int, K: int, F: int, N: int) -> int:
+    return int(_load().w8a8_mlp_workspace_bytes(M, K, F, N))
+
+
+def mlp(X: torch.Tensor, Wp_up: torch.Tensor, sw_up: torch.Tensor, bias_up, Wp_down: torch.Tensor,
+        sw_down: torch.Tensor, bias_down, H=None, out=None, workspace=None, stream=None):
+    """MLP pair Y = down(up(X)) on the W8A8 path, the down layer's row
+    quantisation fed by the up GEMM's row maxima.  Returns (Y, H)."""
+    _cuda2d(X, "X")
+    M, K = X.shape
+    F = Wp_up.shape[0]
+    N = Wp_down.shape[0]
+    if Wp_up.shape[1] != K or Wp_down.shape[1] != F:
+        raise ValueError("shape mismatch: X %s, Wp_up %s, Wp_down %s"
+                         % (tuple(X.shape), tuple(Wp_up.shape), tuple(Wp_down.shape)))
+    if H is None:
+        H = torch.empty((M, F), dtype=torch.bfloat16, device=X.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        need = mlp_workspace_bytes(M, K, F, N)
+        if need == 0:
+            raise UnsupportedShape(4, "mlp workspace size")
+        workspace = torch.empty((need,), dtype=torch.uint8, device=X.device)
+    bu = _dt(bias_up) if bias_up is not None else BF16
+    bdn = _dt(bias_down) if bias_down is not None else BF16
+    _check(_load().w8a8_mlp(_ptr(X), _dt(X), M, K, _ptr(Wp_up), _ptr(sw_up), F, _ptr(bias_up), bu, _ptr(Wp_down),
+                            _ptr(sw_down), N, _ptr(bias_down), bdn, _ptr(H), _ptr(out), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream)), "w8a8_mlp")
+    return out, H
 
 
 LAYOUTS = {"HND": 0, "NHD": 1}

@@ -104,9 +104,12 @@ static_assert(GemmCfg<1>::kStages * GemmCfg<1>::kStageBytes >= kPartialInt4 * 16
 //   kModeBf16  bf16 activations and weights in (the native BF16 linear that
 //              guard-rejected shapes and BF16 layers run), fp32 sums (the
 //              tensor memory chunks added in fp32), Y = bf16(acc + b)
+//   kModeW8A8RowMax  kModeW8A8, and each row's max |Y| gathered into
+//              p.row_amax (the next layer's activation scale, MLP pair)
 constexpr int kModeW8A8 = 0;
 constexpr int kModeS32 = 1;
 constexpr int kModeBf16 = 2;
+constexpr int kModeW8A8RowMax = 3;
 
 // Status bits (same values as W8A8_DEV_* in the public header).
 constexpr uint32_t kDevTimeoutProducer = 0x1;
@@ -129,6 +132,7 @@ struct GemmParams {
     uint32_t* status;          // device status word
     uint32_t* tile_counters;   // [(tiles - dp_tiles) * kPair] arrivals per split (tile, CTA rank)
     int4* partials;            // [tail_units * kPair][kPartialInt4] INT32 partial tiles
+    uint32_t* row_amax;        // [M] (kModeW8A8RowMax): each row's max |Y| as fp32 bits, by atomicMax
     uint64_t wait_limit_ns;
     int32_t skip_loads;        // test hook: producer issues no copies
 };
@@ -224,6 +228,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr uint16_t kBoth = kPair == 2 ? 0x3 : 0x1;
     constexpr bool kOutS32 = kMode == kModeS32;
     constexpr bool kFp32Sums = kMode == kModeBf16;   // sums held as fp32 bit patterns (zero bits = +0.0f)
+    constexpr bool kRowMax = kMode == kModeW8A8RowMax;
+    constexpr bool kScaled = kMode == kModeW8A8 || kRowMax;   // INT8 codes dequantised by sx and sw
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -256,6 +262,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // activation codes, row scales and the workspace header: the set-up
     // above overlaps its tail, nothing below may run before it completes.
     grid_wait_prerequisites();
+    // A kernel that consumes this one's output (the row quantiser of the
+    // next layer) may be scheduled now; it waits for this grid to finish.
+    grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -367,14 +376,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if constexpr (!kOutS32) {
                 const int i = e * 32 + lane;
                 const int n = nb * kBN + i;
-                if constexpr (kMode == kModeW8A8) s_sw[i] = n < p.N ? p.sw[n] : 0.0f;
+                if constexpr (kScaled) s_sw[i] = n < p.N ? p.sw[n] : 0.0f;
                 if (p.bias_mode == 1)
                     s_bias[i] = n < p.N ? static_cast<const float*>(p.bias)[n] : 0.0f;
                 else if (p.bias_mode == 2)
                     s_bias[i] = n < p.N ? __uint_as_float(static_cast<uint32_t>(
                                               static_cast<const uint16_t*>(p.bias)[n]) << 16)
                                         : 0.0f;
-                if (kMode == kModeW8A8 && m < p.M) sxm = p.sx[m];
+                if (kScaled && m < p.M) sxm = p.sx[m];
             }
             int32_t acc[128];
 #pragma unroll
@@ -543,6 +552,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     out = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                                      pack_bf16x2(y[6], y[7]));
                 };
+                // Largest |y| of this thread's row segment (bf16 magnitudes
+                // order like unsigned integers), for the next layer's row
+                // scale.  Rows past M are skipped below; columns past N are 0.
+                uint32_t amax2 = 0;
+                auto fold_amax = [&](const uint4& v) {
+                    amax2 = __vmaxu2(amax2, v.x & 0x7FFF7FFFu);
+                    amax2 = __vmaxu2(amax2, v.y & 0x7FFF7FFFu);
+                    amax2 = __vmaxu2(amax2, v.z & 0x7FFF7FFFu);
+                    amax2 = __vmaxu2(amax2, v.w & 0x7FFF7FFFu);
+                };
                 if constexpr (kPair == 2) {
                     // Stage this warp's 32 rows x 128 columns as two 32 x 64
                     // boxes, one after the other in the warp's 4 KB buffer, in
@@ -561,6 +580,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int c = 0; c < 8; ++c) {
                             uint4 v;
                             dequant8(j * 8 + c, v);
+                            if constexpr (kRowMax) fold_amax(v);
                             *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
                         }
                         fence_proxy_async_smem();
@@ -578,9 +598,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (n < p.N) {
                             uint4 v;
                             dequant8(g, v);
+                            if constexpr (kRowMax) fold_amax(v);
                             *reinterpret_cast<uint4*>(row + n) = v;
                         }
                     }
+                }
+                if (kRowMax && m < p.M) {
+                    const uint32_t a = max(amax2 & 0xFFFFu, amax2 >> 16) << 16;   // fp32 bits of the bf16 max
+                    if (a != 0u) atomicMax(p.row_amax + m, a);
                 }
             }
         }

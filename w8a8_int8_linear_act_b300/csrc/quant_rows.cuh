@@ -227,10 +227,13 @@ __device__ __forceinline__ void quantize_vector(const uint4& vec, const RowScale
 // HBM read).  NV == 0: two passes over the row (for very long rows).
 // `header`, when not NULL, is the workspace header (status word and the
 // GEMM's split-tile counters), cleared by block 0 at the start of a call.
+// `zero_rows`, when not NULL, is a per-row word cleared with the row's scale
+// (the row absmax that the following GEMM gathers for the next layer).
 template <typename TIn, bool kBf16Codes, int NV, int kRowsPerCta>
 __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ? 256 : 1024)) quant_rows_kernel(const TIn* __restrict__ A, int64_t R, int64_t K,
                                                           void* __restrict__ Q, float* __restrict__ S,
-                                                          uint32_t* __restrict__ header)
+                                                          uint32_t* __restrict__ header,
+                                                          uint32_t* __restrict__ zero_rows)
 {
     using IV = InVec<TIn>;
     constexpr int E = IV::kElems;
@@ -263,7 +266,10 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ?
         for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
         const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
         const RowScale rs = row_scale(amax);
-        if (t == 0) S[row] = rs.s;
+        if (t == 0) {
+            S[row] = rs.s;
+            if (zero_rows != nullptr) zero_rows[row] = 0u;
+        }
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int idx = t + i * T;
@@ -273,9 +279,47 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ?
         for (int idx = t; idx < V; idx += T) IV::absmax(load_stream(src + idx), m2);
         const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
         const RowScale rs = row_scale(amax);
-        if (t == 0) S[row] = rs.s;
+        if (t == 0) {
+            S[row] = rs.s;
+            if (zero_rows != nullptr) zero_rows[row] = 0u;
+        }
         for (int idx = t; idx < V; idx += T)
             quantize_vector<TIn, kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+    }
+}
+
+// Codes of bf16 rows whose absmax is already known: the row rule without the
+// reduction, for the layer after a GEMM that gathered each row's max |Y|
+// while writing Y (amax_bits: fp32 bits, 0 for an all-zero row).  One CTA
+// per row; a thread loads up to kU vectors before quantising any, so every
+// warp keeps 16 * kU bytes per lane in flight.  Launched as a programmatic
+// dependent of that GEMM: it waits for the GEMM's results before reading.
+template <bool kBf16Codes, int kU>
+__global__ void __launch_bounds__(256) codes_known_amax_kernel(const __nv_bfloat16* __restrict__ A, int64_t K,
+                                                               const uint32_t* __restrict__ amax_bits,
+                                                               void* __restrict__ Q, float* __restrict__ S)
+{
+    grid_launch_dependents();
+    grid_wait_prerequisites();
+    const int64_t row = blockIdx.x;
+    const RowScale rs = row_scale(__uint_as_float(amax_bits[row]));
+    if (threadIdx.x == 0) S[row] = rs.s;
+    const int V = static_cast<int>(K / 8);
+    const uint4* src = reinterpret_cast<const uint4*>(A + row * K);
+    const int64_t out0 = row * K;
+    for (int base = static_cast<int>(threadIdx.x); base < V; base += kU * static_cast<int>(blockDim.x)) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int idx = base + u * static_cast<int>(blockDim.x);
+            v[u] = idx < V ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int idx = base + u * static_cast<int>(blockDim.x);
+            if (idx < V)
+                quantize_vector<__nv_bfloat16, kBf16Codes>(v[u], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+        }
     }
 }
 

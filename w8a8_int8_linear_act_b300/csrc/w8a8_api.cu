@@ -235,7 +235,8 @@ bool ensure_gemm_ready(DeviceInfo* dev)
     using namespace w8a8;
     if (set_gemm_smem<kModeW8A8, 1>() != cudaSuccess || set_gemm_smem<kModeS32, 1>() != cudaSuccess ||
         set_gemm_smem<kModeBf16, 1>() != cudaSuccess || set_gemm_smem<kModeW8A8, 2>() != cudaSuccess ||
-        set_gemm_smem<kModeS32, 2>() != cudaSuccess || set_gemm_smem<kModeBf16, 2>() != cudaSuccess) {
+        set_gemm_smem<kModeS32, 2>() != cudaSuccess || set_gemm_smem<kModeBf16, 2>() != cudaSuccess ||
+        set_gemm_smem<kModeW8A8RowMax, 1>() != cudaSuccess || set_gemm_smem<kModeW8A8RowMax, 2>() != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -291,11 +292,11 @@ w8a8_status last_launch_status()
 
 template <typename TIn, bool kBf16Codes, int NV, int kRows>
 void launch_quant_cfg(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header, unsigned threads,
-                      cudaStream_t stream)
+                      cudaStream_t stream, uint32_t* zero_rows)
 {
     const int64_t blocks = (R + kRows - 1) / kRows;
     w8a8::quant_rows_kernel<TIn, kBf16Codes, NV, kRows>
-        <<<static_cast<unsigned>(blocks), threads, 0, stream>>>(A, R, K, Q, S, header);
+        <<<static_cast<unsigned>(blocks), threads, 0, stream>>>(A, R, K, Q, S, header, zero_rows);
 }
 
 // Rows of up to 512 16-byte vectors: a warp per row, four rows per CTA, each
@@ -304,36 +305,37 @@ void launch_quant_cfg(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uin
 // row reading it twice.
 template <typename TIn, bool kBf16Codes>
 w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header,
-                               cudaStream_t stream)
+                               cudaStream_t stream, uint32_t* zero_rows)
 {
     constexpr int E = w8a8::InVec<TIn>::kElems;
     const int64_t V = K / E;  // vectors per row
     if (V <= 32)
-        launch_quant_cfg<TIn, kBf16Codes, 1, 4>(A, R, K, Q, S, header, 128, stream);
+        launch_quant_cfg<TIn, kBf16Codes, 1, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
     else if (V <= 64)
-        launch_quant_cfg<TIn, kBf16Codes, 2, 4>(A, R, K, Q, S, header, 128, stream);
+        launch_quant_cfg<TIn, kBf16Codes, 2, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
     else if (V <= 128)
-        launch_quant_cfg<TIn, kBf16Codes, 4, 4>(A, R, K, Q, S, header, 128, stream);
+        launch_quant_cfg<TIn, kBf16Codes, 4, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
     else if (V <= 256)
-        launch_quant_cfg<TIn, kBf16Codes, 8, 4>(A, R, K, Q, S, header, 128, stream);
+        launch_quant_cfg<TIn, kBf16Codes, 8, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
     else if (V <= 512)
-        launch_quant_cfg<TIn, kBf16Codes, 16, 4>(A, R, K, Q, S, header, 128, stream);
+        launch_quant_cfg<TIn, kBf16Codes, 16, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
     else if (V <= 4096) {
         const unsigned T = static_cast<unsigned>(((V + 15) / 16 + 31) / 32 * 32);
-        launch_quant_cfg<TIn, kBf16Codes, 16, 1>(A, R, K, Q, S, header, T, stream);
+        launch_quant_cfg<TIn, kBf16Codes, 16, 1>(A, R, K, Q, S, header, T, stream, zero_rows);
     } else
-        launch_quant_cfg<TIn, kBf16Codes, 0, 1>(A, R, K, Q, S, header, 1024, stream);
+        launch_quant_cfg<TIn, kBf16Codes, 0, 1>(A, R, K, Q, S, header, 1024, stream, zero_rows);
     return last_launch_status();
 }
 
 template <bool kBf16Codes>
 w8a8_status launch_quant(const void* A, int dtype, int64_t R, int64_t K, void* Q, float* S, uint32_t* status,
-                         cudaStream_t stream)
+                         cudaStream_t stream, uint32_t* zero_rows = nullptr)
 {
     if (dtype == W8A8_BF16)
         return launch_quant_typed<__nv_bfloat16, kBf16Codes>(static_cast<const __nv_bfloat16*>(A), R, K, Q, S,
-                                                             status, stream);
-    return launch_quant_typed<float, kBf16Codes>(static_cast<const float*>(A), R, K, Q, S, status, stream);
+                                                             status, stream, zero_rows);
+    return launch_quant_typed<float, kBf16Codes>(static_cast<const float*>(A), R, K, Q, S, status, stream,
+                                                 zero_rows);
 }
 
 w8a8_status check_quant_args(const void* A, int dtype, int64_t R, int64_t K, const void* Q, const float* S)
@@ -374,7 +376,8 @@ w8a8_status launch_codes_to_bf16(const int8_t* Qi, uint16_t* Qb, int64_t n, uint
 template <int kMode>
 w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t* Wp, int64_t M, int64_t N,
                         int64_t K, const float* sx, const float* sw, const void* bias, int bias_mode, void* out,
-                        uint8_t* ws_aligned, const WsLayout& L, int64_t slots, cudaStream_t stream)
+                        uint8_t* ws_aligned, const WsLayout& L, int64_t slots, cudaStream_t stream,
+                        uint32_t* row_amax = nullptr)
 {
     if (!ensure_gemm_ready(dev)) return W8A8_ERR_CUDA;
     const GemmPlan g = choose_plan(M, N, K, dev->num_sms, dev->pair_workers, slots);
@@ -410,6 +413,7 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     p.dp_tiles = static_cast<int32_t>(g.dp_tiles);
     p.splits = g.splits;
     p.tail_units = static_cast<int32_t>(g.tail_units);
+    p.row_amax = row_amax;
     // A programmatic dependent of the kernel before it in the stream (the
     // quantiser that writes its codes): its set-up overlaps that kernel's
     // tail, and it waits on the device for its results (griddepcontrol).
@@ -440,6 +444,53 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
         return W8A8_ERR_CUDA;
     }
     return last_launch_status();
+}
+
+// The next layer's codes from rows whose absmax the previous GEMM gathered,
+// as a programmatic dependent of that GEMM (it waits on the device for the
+// GEMM's Y and row maxima).
+w8a8_status launch_codes_known_amax(const uint16_t* H, int64_t M, int64_t F, const uint32_t* amax, uint16_t* codes,
+                                    float* sx, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, w8a8::codes_known_amax_kernel<true, 8>,
+                                               reinterpret_cast<const __nv_bfloat16*>(H), F, amax,
+                                               static_cast<void*>(codes), sx);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    return last_launch_status();
+}
+
+// Workspace of w8a8_mlp, relative to the first 1024-byte boundary:
+//   header 1 KB (status word, split-tile counters; both GEMMs use them in turn)
+//   sx_x [M], codes_x [M][K] bf16      the up layer's activation
+//   amax_h [M] fp32 bits, sx_h [M], codes_h [M][F] bf16   the down layer's
+//   slots  INT32 partial tiles, shared by the two GEMMs (one runs at a time)
+struct MlpLayout {
+    WsLayout up;        // status_off, sx_off, codes_off; slots_off = the shared slots
+    size_t amax_off, sxh_off, codesh_off;
+};
+
+bool mlp_layout(int64_t M, int64_t K, int64_t F, MlpLayout* L)
+{
+    if (!ws_layout(M, K, &L->up) || F < 1 || F > INT32_MAX) return false;
+    const size_t after_x = L->up.slots_off;
+    L->amax_off = after_x;
+    L->sxh_off = L->amax_off + align_up(static_cast<size_t>(M) * 4u, kAlign);
+    L->codesh_off = L->sxh_off + align_up(static_cast<size_t>(M) * 4u, kAlign);
+    L->up.slots_off = L->codesh_off + align_up(static_cast<size_t>(M) * static_cast<size_t>(F) * 2u, kAlign);
+    L->up.min_total = kAlign + L->up.slots_off;
+    return true;
 }
 
 // Copy streams and events of w8a8_linear_host, created once per device (with
@@ -856,6 +907,65 @@ w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64
     if (x_dtype == W8A8_BF16)
         return launch_blocks_typed<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(X), g, blocks, Xq, scales, s);
     return launch_blocks_typed<float>(static_cast<const float*>(X), g, blocks, Xq, scales, s);
+}
+
+size_t w8a8_mlp_workspace_bytes(int64_t M, int64_t K, int64_t F, int64_t N)
+{
+    if (guard_reasons(M, F, K, W8A8_BF16, W8A8_BF16) != 0 || guard_reasons(M, N, F, W8A8_BF16, W8A8_BF16) != 0)
+        return 0;
+    MlpLayout L;
+    if (!mlp_layout(M, K, F, &L)) return 0;
+    const GemmPlan gu = current_plan(M, F, K, INT64_MAX);
+    const GemmPlan gd = current_plan(M, N, F, INT64_MAX);
+    const int64_t su = gu.tail_units * gu.pair, sd = gd.tail_units * gd.pair;
+    return L.up.min_total + static_cast<size_t>(su > sd ? su : sd) * kSlotBytes;
+}
+
+w8a8_status w8a8_mlp(const void* X, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp_up, const float* sw_up,
+                     int64_t F, const void* bias_up, int bias_up_dtype, const uint16_t* Wp_down,
+                     const float* sw_down, int64_t N, const void* bias_down, int bias_down_dtype, uint16_t* H,
+                     uint16_t* Y, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!X || !Wp_up || !sw_up || !Wp_down || !sw_down || !H || !Y || M < 0 || K < 0 || F < 0 || N < 0)
+        return W8A8_ERR_INVALID_ARG;
+    if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (bias_up && bias_up_dtype != W8A8_F32 && bias_up_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (bias_down && bias_down_dtype != W8A8_F32 && bias_down_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (guard_reasons(M, F, K, x_dtype, bias_up ? bias_up_dtype : W8A8_F32) != 0 ||
+        guard_reasons(M, N, F, W8A8_BF16, bias_down ? bias_down_dtype : W8A8_F32) != 0)
+        return W8A8_ERR_UNSUPPORTED_SHAPE;
+    MlpLayout L;
+    if (!ws || !mlp_layout(M, K, F, &L) || ws_bytes < L.up.min_total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(X, 16) || !aligned(Wp_up, 16) || !aligned(sw_up, 16) || !aligned(Wp_down, 16) ||
+        !aligned(sw_down, 16) || !aligned(H, 16) || !aligned(Y, 16) || !aligned(ws, 16))
+        return W8A8_ERR_ALIGNMENT;
+    if ((bias_up && !aligned(bias_up, 16)) || (bias_down && !aligned(bias_down, 16))) return W8A8_ERR_ALIGNMENT;
+    int devno = 0;
+    DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(&devno));
+    if (!dev) return W8A8_ERR_NO_DEVICE;
+    uint8_t* w = ws_base(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* header = reinterpret_cast<uint32_t*>(w + L.up.status_off);
+    uint32_t* amax = reinterpret_cast<uint32_t*>(w + L.amax_off);
+    float* sxh = reinterpret_cast<float*>(w + L.sxh_off);
+    uint16_t* codesh = reinterpret_cast<uint16_t*>(w + L.codesh_off);
+    const int64_t slots = ws_slots(L.up, ws_bytes);
+    // 1. the up layer's activation codes; also clears the header and the
+    //    row maxima the up GEMM gathers
+    w8a8_status st = launch_quant<true>(X, x_dtype, M, K, w + L.up.codes_off, reinterpret_cast<float*>(w + L.up.sx_off),
+                                        header, s, amax);
+    if (st != W8A8_OK) return st;
+    // 2. H = up layer, with each row's max |H|
+    st = launch_gemm<w8a8::kModeW8A8RowMax>(dev, reinterpret_cast<const uint16_t*>(w + L.up.codes_off), Wp_up, M, F, K,
+                                      reinterpret_cast<const float*>(w + L.up.sx_off), sw_up, bias_up,
+                                      bias_up ? (bias_up_dtype == W8A8_F32 ? 1 : 2) : 0, H, w, L.up, slots, s, amax);
+    if (st != W8A8_OK) return st;
+    // 3. the down layer's codes from H and the gathered maxima (no reduction)
+    st = launch_codes_known_amax(H, M, F, amax, codesh, sxh, s);
+    if (st != W8A8_OK) return st;
+    // 4. Y = down layer
+    return launch_gemm<w8a8::kModeW8A8>(dev, codesh, Wp_down, M, N, F, sxh, sw_down, bias_down,
+                                        bias_down ? (bias_down_dtype == W8A8_F32 ? 1 : 2) : 0, Y, w, L.up, slots, s);
 }
 
 w8a8_status w8a8_read_status(const void* ws, void* stream, uint32_t* device_bits)
