@@ -47,7 +47,7 @@ FLUSH_BYTES = 256 << 20
 # them, and the bench reports null traffic when the sources have changed since.
 GEMM_SOURCES = ["w8a8_int8_linear_act_b300/csrc/gemm_tcgen05.cuh",
                 "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh"]
-GEMM_TRAFFIC = {"87fb347344a746fa": 169.65e6}
+GEMM_TRAFFIC = {"73dd1a18aa8b88ef": 164.14e6}
 
 
 def sources_digest(paths):
@@ -489,6 +489,8 @@ def run_ours(args):
                 "note": "the guard's native BF16 fallback on this shape, header clear + GEMM, L2 flushed"}
         del Xb, Wb, bb, wsb
 
+    pk_hbm = peaks()["hbm_gbs"]
+
     # SageSLA's per-block INT8 Query/Key quantisation at the video branch's
     # attention shape (32 heads of 128 over this workload's tokens), each call
     # timed alone after a flush.
@@ -515,6 +517,41 @@ def run_ours(args):
             qk[name] = {"block_tokens": bt, "ms": q_ms, "achieved": gbs, "frac": gbs / qk["peak"],
                         "algorithmic_bytes": nbytes}
         del Xqk
+
+    # The norm + modulation prologue fused into the activation quantisation
+    # (RMS norm, bf16 scale and shift) on this workload: the kernel alone
+    # (int8 codes) and the whole layer against the plain linear step.
+    normp = None
+    if X.dtype == torch.bfloat16:
+        gn = torch.Generator().manual_seed(21)
+        scn = (torch.randn(K, generator=gn) * 0.1).to(torch.bfloat16).to(dev)
+        shn = (torch.randn(K, generator=gn) * 0.1).to(torch.bfloat16).to(dev)
+
+        def timed(fn, n):
+            for _ in range(3):
+                flush.zero_()
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            for a, b_ in ev:
+                flush.zero_()
+                a.record(stream)
+                fn()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(a.elapsed_time(b_) for a, b_ in ev)
+
+        n_it = min(args.steps, 200)
+        k_ms = timed(lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn, stream=stream), n_it)
+        nl_ms = timed(lambda: w8.norm_linear(Xd, Wp, sw, bd, "rms", 1e-6, scn, shn, out=Y, workspace=ws,
+                                             stream=stream), n_it)
+        nbytes = M * K * 2 + M * K + M * 4 + 2 * K * 2
+        normp = {"kernel": "norm_quant_rows_kernel (RMS norm, bf16 modulation, int8 codes)", "ms": k_ms,
+                 "achieved": nbytes / (k_ms * 1e-3) / 1e9, "unit": "GB/s", "peak": pk_hbm,
+                 "frac": nbytes / (k_ms * 1e-3) / 1e9 / pk_hbm, "algorithmic_bytes": nbytes,
+                 "norm_linear_ms": nl_ms, "norm_linear_tops": case.ops / (nl_ms * 1e-3) / 1e12,
+                 "linear_step_ms": step_ms,
+                 "note": "w8a8_norm_linear = the prologue + GEMM in one call; the unfused form would add a "
+                         "write and a read of the modulated activation (2 B each per element)"}
 
     # The MLP pair at the MLP workload's sizes (6144 x 4096 -> 16384 -> 4096):
     # w8a8_mlp (the down layer's codes from the up GEMM's gathered row maxima)
@@ -633,6 +670,7 @@ def run_ours(args):
             "bf16_fallback": bf16,
             "qk_block_quant": qk,
             "mlp_pair": mlp,
+            "norm_prologue": normp,
             "clocks": clocks,
             "wall_s_timed": t_wall,
         }

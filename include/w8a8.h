@@ -312,6 +312,35 @@ W8A8_API w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, c
                                       void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Normalisation and modulation fused into the activation quantisation, the
+ * prologue of a linear layer (zhidx TurboT2VA article, section 01: the
+ * inference stack fuses normalisation and modulation to cut intermediate
+ * reads and writes; arXiv paper, appendix C).  Per row x of X [M][K] bf16:
+ *   mu = 0 (W8A8_NORM_RMS) or fp32(sum x / K) (W8A8_NORM_LAYER)
+ *   r  = 1 / sqrt(fp32(sum (x - mu)^2 / K) + eps)   (correctly rounded)
+ *   y  = bf16_rne(((x - mu) * r) * (1 + scale) + shift)   (fp32 steps)
+ * then y is quantised by the row rule (as w8a8_quantize_act).  scale and
+ * shift are optional [K] vectors of `mod_dtype` (F32 or BF16, 16-byte
+ * aligned), shared by all rows; NULL omits that step.  The fp32 sums run
+ * in an order of the kernel's choosing.  K % 16 == 0, K <= W8A8_NORM_MAX_K.
+ *
+ * w8a8_norm_quantize_act: codes Xq [M][K] int8 and scales sx [M]; Y_mod
+ *   (nullable) also receives y [M][K] bf16.
+ * w8a8_norm_linear: the same prologue feeding the W8A8 GEMM, with the
+ *   arguments, workspace and errors of w8a8_linear (X bf16).
+ * ------------------------------------------------------------------------- */
+#define W8A8_NORM_RMS 1
+#define W8A8_NORM_LAYER 2
+#define W8A8_NORM_MAX_K 32768
+W8A8_API w8a8_status w8a8_norm_quantize_act(const uint16_t* X, int64_t M, int64_t K, int norm, float eps,
+                                            const void* scale, const void* shift, int mod_dtype, uint16_t* Y_mod,
+                                            int8_t* Xq, float* sx, void* stream);
+W8A8_API w8a8_status w8a8_norm_linear(const uint16_t* X, int64_t M, int64_t K, int norm, float eps,
+                                      const void* scale, const void* shift, int mod_dtype, const uint16_t* Wp,
+                                      const float* sw, int64_t N, const void* bias, int bias_dtype, uint16_t* Y,
+                                      void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * MLP pair: Y = down(up(X)), both layers on the W8A8 path, with the down
  * layer's per-row activation quantisation fed by the up layer's epilogue.
  * Each layer is the linear above (zhidx TurboT2VA article, section 01 item

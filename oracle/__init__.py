@@ -24,6 +24,10 @@ Functions:
                                sum_k X W + b in float64 (bf16 products are exact in
                                float64), and sum_k |X W| for the fp32-accumulation bound
   bf16_linear_tolerance(..) -> that bound, per output
+  norm_modulate_f64(X, kind, eps, scale, shift)
+                            -> the normalised and modulated rows in float64 (RMS norm or
+                               LayerNorm, then x * (1 + scale) + shift), with mean and 1/std
+  norm_quantize(X, ...)     -> codes and scales of bf16_rne of those rows (quantize_rows)
   quantize_qk_blocks(X, bt, layout)
                             -> per-block INT8 codes and scales of attention Query/Key:
                                quantize_rows applied to each block of bt tokens of one
@@ -59,6 +63,8 @@ def _load():
         lib.oracle_epilogue.restype = None
         lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
         lib.oracle_bf16_rne.restype = ctypes.c_uint16
+        lib.oracle_bf16_rne_array.argtypes = [_p, _i64, _p]
+        lib.oracle_bf16_rne_array.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -164,9 +170,10 @@ def epilogue(acc: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias=None):
 
 def bf16_rne(x) -> np.ndarray:
     """bf16 round-to-nearest-even of float32 values, as uint16 bit patterns."""
-    x = np.asarray(x, dtype=np.float32)
-    f = _load().oracle_bf16_rne
-    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_bf16_rne_array(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -259,4 +266,43 @@ def quantize_qk_blocks(X: np.ndarray, block_tokens: int, layout: str = "HND"):
         q[:, :, t0:t1, :] = qj.reshape(B, H, t1 - t0, D)
         s[:, :, j] = sj.reshape(B, H)
     return (q if layout == "HND" else np.ascontiguousarray(q.transpose(0, 2, 1, 3))), s
+
+
+def norm_modulate_f64(X_bits: np.ndarray, kind: str, eps: float, scale=None, shift=None):
+    """Normalisation and modulation before a linear layer, as the TurboT2VA
+    pages fuse them (zhidx article, section 01: normalisation and modulation
+    fused to cut intermediate reads and writes; arXiv paper, appendix C).
+
+    Per row x of X (bf16 bits [M, K]), in float64:
+      kind "rms":   mu = 0;             v = mean(x^2)
+      kind "layer": mu = mean(x);       v = mean((x - mu)^2)
+      r = 1 / sqrt(v + eps)
+      y = (x - mu) * r * (1 + scale) + shift     (scale, shift: [K] or None)
+    Returns (y [M, K], mu [M], r [M]), all float64."""
+    x = bf16_bits_to_f32(np.ascontiguousarray(X_bits)).astype(np.float64)
+    K = x.shape[1]
+    if kind == "rms":
+        mu = np.zeros(x.shape[0])
+    elif kind == "layer":
+        mu = x.sum(axis=1) / K
+    else:
+        raise ValueError("kind must be 'rms' or 'layer'")
+    d = x - mu[:, None]
+    r = 1.0 / np.sqrt((d * d).sum(axis=1) / K + eps)
+    y = d * r[:, None]
+    if scale is not None:
+        y = y * (1.0 + np.asarray(scale, dtype=np.float64))[None, :]
+    if shift is not None:
+        y = y + np.asarray(shift, dtype=np.float64)[None, :]
+    return y, mu, r
+
+
+def norm_quantize(X_bits: np.ndarray, kind: str, eps: float, scale=None, shift=None):
+    """The rows above rounded to bf16 (nearest even) and quantised by the row
+    rule (zhidx article, section 01 item 3).  Returns (y_bf16 bits, codes,
+    scales, y float64)."""
+    y, _, _ = norm_modulate_f64(X_bits, kind, eps, scale, shift)
+    yb = bf16_rne(y.astype(np.float32).ravel()).reshape(y.shape)
+    q, s = quantize_rows(yb)
+    return yb, q, s, y
 

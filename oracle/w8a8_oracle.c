@@ -64,6 +64,12 @@ uint16_t oracle_bf16_rne(float f)
     return (uint16_t)upper;
 }
 
+/* The same rounding over an array (one call instead of one per value). */
+void oracle_bf16_rne_array(const float* x, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne(x[i]);
+}
+
 float oracle_bf16_to_float(uint16_t h) { return bf16_bits_to_float(h); }
 
 /* ---- round half to even, written out ------------------------------------

@@ -278,3 +278,20 @@ def test_mlp_workspace_and_argument_errors(lib):
     assert call(a11=12) == 4
     assert call(a17=64) == 5
     assert call(a15=ctypes.c_void_p(0x10008)) == 3
+
+
+def test_norm_argument_errors(lib):
+    p = ctypes.c_void_p(0x10000)
+    null = None
+    f = lib.w8a8_norm_quantize_act
+    assert f(null, 4, 64, 1, 1e-6, null, null, 1, null, p, p, null) == 1
+    assert f(p, 4, 64, 3, 1e-6, null, null, 1, null, p, p, null) == 1         # unknown norm
+    assert f(p, 4, 64, 1, -1.0, null, null, 1, null, p, p, null) == 1         # negative eps
+    assert f(p, 4, 64, 1, 1e-6, p, null, 7, null, p, p, null) == 2            # modulation dtype
+    assert f(p, 4, 72, 1, 1e-6, null, null, 1, null, p, p, null) == 4         # K % 16
+    assert f(p, 4, 32784, 1, 1e-6, null, null, 1, null, p, p, null) == 4      # K > 32768
+    assert f(p, 4, 64, 1, 1e-6, ctypes.c_void_p(0x10008), null, 1, null, p, p, null) == 3
+    assert f(p, 4, 64, 1, 1e-6, null, null, 1, null, null, p, null) == 1
+    g = lib.w8a8_norm_linear
+    assert g(p, 4, 64, 1, 1e-6, null, null, 1, p, p, 12, null, 1, p, p, 1 << 20, null) == 4
+    assert g(p, 4, 64, 1, 1e-6, null, null, 1, p, p, 128, null, 1, p, p, 64, null) == 5

@@ -480,3 +480,83 @@ def test_qk_blocks_are_independent_and_saturate():
     for h in range(2):
         for j in range(3):
             assert np.abs(q[0, h, 4 * j:4 * j + 4].astype(np.int32)).max() == 127
+
+
+# ---------------------------------------------------------------- normalisation + modulation
+
+def _bits(a):
+    return oracle.bf16_rne(np.asarray(a, dtype=np.float32))
+
+
+def test_norm_brute_force():
+    """Pure-Python restatement of both norms with modulation on small rows."""
+    import math
+    rng = np.random.default_rng(31)
+    xb = _bits(rng.standard_normal((3, 16)) * 2)
+    x = oracle.bf16_bits_to_f32(xb).astype(np.float64)
+    sc = rng.standard_normal(16) * 0.1
+    sh = rng.standard_normal(16) * 0.1
+    for kind in ("rms", "layer"):
+        y, mu, r = oracle.norm_modulate_f64(xb, kind, 1e-6, sc, sh)
+        for m in range(3):
+            row = [float(v) for v in x[m]]
+            mean = math.fsum(row) / 16 if kind == "layer" else 0.0
+            var = math.fsum((v - mean) ** 2 for v in row) / 16
+            rr = 1.0 / math.sqrt(var + 1e-6)
+            for k in range(16):
+                want = (row[k] - mean) * rr * (1.0 + sc[k]) + sh[k]
+                assert abs(y[m, k] - want) <= 1e-12 * max(1.0, abs(want))
+            assert abs(mu[m] - mean) <= 1e-12 and abs(r[m] - rr) <= 1e-12 * rr
+
+
+def test_norm_closed_forms():
+    """A constant row c under RMS norm gives c / sqrt(c^2 + eps); a row of two
+    values a, b (half each) under LayerNorm gives +-1 / sqrt(1 + eps / d^2)
+    with d = (a - b) / 2."""
+    c, eps = 1.5, 1e-3
+    y, _, _ = oracle.norm_modulate_f64(_bits(np.full((1, 32), c)), "rms", eps)
+    assert np.allclose(y, c / np.sqrt(c * c + eps), rtol=1e-14, atol=0)
+    a, b = 3.0, -1.0
+    row = np.array([a, b] * 16)
+    y, mu, _ = oracle.norm_modulate_f64(_bits(row[None, :]), "layer", eps)
+    d = (a - b) / 2
+    assert mu[0] == (a + b) / 2
+    assert np.allclose(y[0], np.where(row == a, 1.0, -1.0) / np.sqrt(1.0 + eps / (d * d)), rtol=1e-14, atol=0)
+
+
+def test_norm_invariances_and_modulation():
+    """LayerNorm ignores a constant offset; RMS norm ignores a power-of-two
+    gain (eps = 0); scale = -1 leaves exactly the shift; RMS output has unit
+    mean square (eps = 0)."""
+    rng = np.random.default_rng(32)
+    xb = _bits(rng.integers(-64, 64, size=(4, 64)) / 16.0)
+    x = oracle.bf16_bits_to_f32(xb).astype(np.float64)
+    y1, _, _ = oracle.norm_modulate_f64(xb, "layer", 0.0)
+    y2, _, _ = oracle.norm_modulate_f64(_bits(x + 8.0), "layer", 0.0)
+    assert np.allclose(y1, y2, rtol=0, atol=1e-12)
+    y3, _, _ = oracle.norm_modulate_f64(xb, "rms", 0.0)
+    y4, _, _ = oracle.norm_modulate_f64(_bits(x * 4.0), "rms", 0.0)
+    assert np.array_equal(y3, y4)
+    assert np.allclose((y3 * y3).mean(axis=1), 1.0, rtol=1e-13)
+    sh = rng.standard_normal(64)
+    y5, _, _ = oracle.norm_modulate_f64(xb, "rms", 1e-6, np.full(64, -1.0), sh)
+    assert np.array_equal(y5, np.broadcast_to(sh, y5.shape))
+
+
+def test_norm_quantize_composes_the_pinned_parts():
+    """norm_quantize is bf16_rne of the float64 rows followed by the pinned
+    row quantiser."""
+    rng = np.random.default_rng(33)
+    xb = _bits(rng.standard_normal((5, 48)))
+    yb, q, s, y = oracle.norm_quantize(xb, "layer", 1e-5, rng.standard_normal(48) * 0.1, None)
+    assert np.array_equal(yb, oracle.bf16_rne(y.astype(np.float32)))
+    q2, s2 = oracle.quantize_rows(yb)
+    assert np.array_equal(q, q2) and np.array_equal(s, s2)
+
+
+def test_bf16_rne_array_matches_scalar():
+    rng = np.random.default_rng(34)
+    v = np.concatenate([rng.standard_normal(5000).astype(np.float32),
+                        np.array([0.0, -0.0, 1.00390625, 1.01171875, np.inf, -np.inf, 3.4e38], dtype=np.float32)])
+    lib = oracle._load()
+    assert np.array_equal(oracle.bf16_rne(v), np.array([lib.oracle_bf16_rne(float(t)) for t in v], dtype=np.uint16))

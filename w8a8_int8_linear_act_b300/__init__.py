@@ -23,7 +23,8 @@ __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
     "quantize_act", "pack_weight", "workspace_bytes", "workspace_min_bytes", "gemm_plan", "linear", "linear_quant_stage",
     "linear_gemm_stage", "gemm_s32", "linear_noalloc", "linear_host", "bf16_linear", "bf16_linear_supported",
-    "bf16_linear_workspace_bytes", "quantize_qk_blocks", "mlp", "mlp_workspace_bytes", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
+    "bf16_linear_workspace_bytes", "quantize_qk_blocks", "mlp", "mlp_workspace_bytes", "norm_quantize_act",
+    "norm_linear", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
     "W8A8Linear", "GuardedLinear", "F32", "BF16", "MAX_K",
 ]
 
@@ -88,6 +89,8 @@ def _load():
         "w8a8_bf16_linear": ([p, i64, i64, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_quantize_qk_blocks": ([p, i32, i64, i64, i64, i64, i32, i64, p, p, p], i32),
         "w8a8_mlp_workspace_bytes": ([i64, i64, i64, i64], sz),
+        "w8a8_norm_quantize_act": ([p, i64, i64, i32, ctypes.c_float, p, p, i32, p, p, p, p], i32),
+        "w8a8_norm_linear": ([p, i64, i64, i32, ctypes.c_float, p, p, i32, p, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_mlp": ([p, i32, i64, i64, p, p, i64, p, i32, p, p, i64, p, i32, p, p, p, sz, p], i32),
         "w8a8_read_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
@@ -362,6 +365,55 @@ def mlp(X: torch.Tensor, Wp_up: torch.Tensor, sw_up: torch.Tensor, bias_up, Wp_d
                             _ptr(sw_down), N, _ptr(bias_down), bdn, _ptr(H), _ptr(out), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream)), "w8a8_mlp")
     return out, H
+
+
+NORMS = {"rms": 1, "layer": 2}
+
+
+def _mod_dtype(scale, shift):
+    t = scale if scale is not None else shift
+    if t is None:
+        return BF16
+    if scale is not None and shift is not None and scale.dtype != shift.dtype:
+        raise TypeError("scale and shift must share a dtype")
+    return _dt(t)
+
+
+def norm_quantize_act(X: torch.Tensor, norm: str = "rms", eps: float = 1e-6, scale=None, shift=None,
+                      want_y: bool = False, stream=None):
+    """RMS norm or LayerNorm of each row of X (bf16 [M, K]), modulated by
+    (1 + scale) and shift ([K] or None), rounded to bf16 and quantised per
+    row.  Returns (Xq int8, sx float32) or (Xq, sx, y bf16) with want_y."""
+    _cuda2d(X, "X")
+    if X.dtype != torch.bfloat16:
+        raise TypeError("norm_quantize_act takes bfloat16 X")
+    M, K = X.shape
+    Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    y = torch.empty((M, K), dtype=torch.bfloat16, device=X.device) if want_y else None
+    _check(_load().w8a8_norm_quantize_act(_ptr(X), M, K, NORMS[norm], eps, _ptr(scale), _ptr(shift),
+                                          _mod_dtype(scale, shift), _ptr(y), _ptr(Xq), _ptr(sx), _stream(stream)),
+           "w8a8_norm_quantize_act")
+    return (Xq, sx, y) if want_y else (Xq, sx)
+
+
+def norm_linear(X: torch.Tensor, Wp: torch.Tensor, sw: torch.Tensor, bias=None, norm: str = "rms",
+                eps: float = 1e-6, scale=None, shift=None, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """The W8A8 linear with the norm + modulation prologue fused into its
+    activation quantisation: Y = linear(bf16(norm(X) * (1 + scale) + shift))."""
+    _cuda2d(X, "X")
+    M, K = X.shape
+    N = Wp.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        workspace = torch.empty((workspace_bytes(M, N, K),), dtype=torch.uint8, device=X.device)
+    bdt = _dt(bias) if bias is not None else BF16
+    _check(_load().w8a8_norm_linear(_ptr(X), M, K, NORMS[norm], eps, _ptr(scale), _ptr(shift),
+                                    _mod_dtype(scale, shift), _ptr(Wp), _ptr(sw), N, _ptr(bias), bdt, _ptr(out),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "w8a8_norm_linear")
+    return out
 
 
 LAYOUTS = {"HND": 0, "NHD": 1}

@@ -181,14 +181,6 @@ __device__ __forceinline__ void epi_barrier()
     asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(32 * kEpiWarps) : "memory");
 }
 
-// Two floats rounded to bf16 (nearest, ties to even) in one instruction;
-// `lo` in the low half.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 template <int kMode, int kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_w8a8_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,

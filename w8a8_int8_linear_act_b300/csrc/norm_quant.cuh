@@ -1,0 +1,228 @@
+// Normalisation and modulation fused into the per-row activation
+// quantisation, the prologue of a linear layer in the joint Transformer
+// (zhidx TurboT2VA article, section 01: normalisation, modulation, gated
+// residual and rotary embedding are fused to cut intermediate reads and
+// writes; arXiv paper, appendix C "Fused Multimodal Transformer
+// Operations").  Per row x of K bf16 values:
+//
+//   RMS norm:   mu = 0
+//   LayerNorm:  mu = fp32(sum_k x_k / K)
+//   v   = fp32(sum_k (x_k - mu)^2 / K)
+//   r   = 1 / sqrt(v + eps)                     (correctly rounded fp32)
+//   y_k = bf16_rne(((x_k - mu) * r) * (1 + scale_k) + shift_k)
+//
+// each step one fp32 operation rounded to nearest (the sums in any order);
+// scale and shift are optional [K] vectors (adaLN-style modulation shared by
+// all rows).  y is then quantised by the row rule of quant_rows.cuh, and
+// optionally also written out.  The unfused form would write y (2 B per
+// element) and read it back for the quantiser; here the row is read once.
+//
+// Structure: as the quantiser (a warp per row, four rows per CTA, up to 16
+// vectors per lane, for K <= 4096; a CTA per row up to 32768), with the row
+// held in registers through three reductions: the sum (LayerNorm), the sum
+// of squared deviations, and the absmax of y.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "quant_rows.cuh"
+
+namespace w8a8 {
+
+constexpr int kNormRms = 1;
+constexpr int kNormLayer = 2;
+
+struct NormParams {
+    float eps;
+    const void* scale;     // [K] or nullptr
+    const void* shift;     // [K] or nullptr
+    int32_t mod_f32;       // scale/shift dtype: 1 fp32, 0 bf16
+    uint16_t* y_out;       // [R][K] bf16 y, or nullptr
+};
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Block-wide sum; every thread gets the result.  `red` is used by this
+// reduction alone (the callers give each reduction its own array).
+__device__ __forceinline__ float block_sum(float v, float* red)
+{
+    v = warp_sum(v);
+    const int nwarps = blockDim.x >> 5;
+    if (nwarps == 1) return v;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = 0.0f;
+    for (int w = 0; w < nwarps; ++w) s = __fadd_rn(s, red[w]);
+    return s;
+}
+
+// Pairwise sum of eight partial sums.
+__device__ __forceinline__ float sum8(const float (&p)[8])
+{
+    return __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), __fadd_rn(p[2], p[3])),
+                     __fadd_rn(__fadd_rn(p[4], p[5]), __fadd_rn(p[6], p[7])));
+}
+
+// The eight modulation values of vector idx (elements 8 idx .. 8 idx + 7)
+// as loaded: one 16-byte vector for bf16, two for fp32.
+struct ModVec {
+    uint4 a, b;
+};
+
+__device__ __forceinline__ ModVec load_mod(const void* p, int32_t f32, int idx)
+{
+    ModVec m;
+    if (f32) {
+        const uint4* q = static_cast<const uint4*>(p) + 2 * idx;
+        m.a = __ldg(q);
+        m.b = __ldg(q + 1);
+    } else {
+        m.a = __ldg(static_cast<const uint4*>(p) + idx);
+        m.b = make_uint4(0, 0, 0, 0);
+    }
+    return m;
+}
+
+__device__ __forceinline__ void unpack_mod(const ModVec& m, int32_t f32, float (&out)[8])
+{
+    if (f32) {
+        out[0] = __uint_as_float(m.a.x); out[1] = __uint_as_float(m.a.y);
+        out[2] = __uint_as_float(m.a.z); out[3] = __uint_as_float(m.a.w);
+        out[4] = __uint_as_float(m.b.x); out[5] = __uint_as_float(m.b.y);
+        out[6] = __uint_as_float(m.b.z); out[7] = __uint_as_float(m.b.w);
+    } else {
+        InVec<__nv_bfloat16>::unpack(m.a, out);
+    }
+}
+
+// Hides the packed row from the compiler between passes, so that each pass
+// unpacks it again (two bf16 per register) instead of keeping all K/32
+// unpacked floats of a lane live across the reductions.
+template <int NV>
+__device__ __forceinline__ void keep_packed(uint4 (&v)[NV])
+{
+#pragma unroll
+    for (int i = 0; i < NV; ++i) asm volatile("" : "+r"(v[i].x), "+r"(v[i].y), "+r"(v[i].z), "+r"(v[i].w));
+}
+
+template <bool kBf16Codes, int NV, int kRowsPerCta, int kNorm>
+__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256)
+    norm_quant_rows_kernel(const __nv_bfloat16* __restrict__ A, int64_t R, int64_t K, NormParams np,
+                           void* __restrict__ Q, float* __restrict__ S, uint32_t* __restrict__ header)
+{
+    using IV = InVec<__nv_bfloat16>;
+    __shared__ float red_sum[32], red_sq[32], red_max[32];
+
+    grid_launch_dependents();
+    if (header != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
+
+    const int64_t row = kRowsPerCta > 1 ? static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5)
+                                        : static_cast<int64_t>(blockIdx.x);
+    if (kRowsPerCta > 1 && row >= R) return;   // warp-uniform; no block-wide barrier follows
+    const int T = kRowsPerCta > 1 ? 32 : static_cast<int>(blockDim.x);
+    const int t = kRowsPerCta > 1 ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
+    const int V = static_cast<int>(K / 8);
+    const uint4* src = reinterpret_cast<const uint4*>(A + row * K);
+    const int64_t out0 = row * K;
+    const float kf = static_cast<float>(K);
+
+    uint4 v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int idx = t + i * T;
+        v[i] = (idx < V) ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
+    }
+    // The first modulation vectors, in flight during the reductions.
+    const bool has_sc = np.scale != nullptr, has_sh = np.shift != nullptr;
+    ModVec nsc = {}, nsh = {};
+    if (t < V) {
+        if (has_sc) nsc = load_mod(np.scale, np.mod_f32, t);
+        if (has_sh) nsh = load_mod(np.shift, np.mod_f32, t);
+    }
+
+    // Each sum runs in eight independent partial sums per thread (one per
+    // element position of a vector), so the adds do not form one long
+    // dependent chain; the partials are then added pairwise.
+    float mu = 0.0f;
+    if constexpr (kNorm == kNormLayer) {
+        float p8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            float x[8];
+            IV::unpack(v[i], x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p8[e] = __fadd_rn(p8[e], x[e]);   // padding vectors are zero
+        }
+        float s = sum8(p8);
+        s = kRowsPerCta > 1 ? warp_sum(s) : block_sum(s, red_sum);
+        mu = __fdiv_rn(s, kf);
+        keep_packed(v);
+    }
+    float q8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        if (t + i * T < V) {
+            float x[8];
+            IV::unpack(v[i], x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float d = kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e];
+                q8[e] = __fmaf_rn(d, d, q8[e]);
+            }
+        }
+    }
+    float q = sum8(q8);
+    q = kRowsPerCta > 1 ? warp_sum(q) : block_sum(q, red_sq);
+    keep_packed(v);
+    const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(q, kf), np.eps));
+
+    // y, rounded to bf16, replaces x in the registers.  The modulation
+    // vectors of the next vector are fetched while this one is computed (the
+    // same K-vectors for every row, so they come from L1).
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int idx = t + i * T;
+        if (idx < V) {
+            const ModVec csc = nsc, csh = nsh;
+            if (i + 1 < NV && idx + T < V) {
+                if (has_sc) nsc = load_mod(np.scale, np.mod_f32, idx + T);
+                if (has_sh) nsh = load_mod(np.shift, np.mod_f32, idx + T);
+            }
+            float x[8], sc[8], sh[8];
+            IV::unpack(v[i], x);
+            if (has_sc) unpack_mod(csc, np.mod_f32, sc);
+            if (has_sh) unpack_mod(csh, np.mod_f32, sh);
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float z = __fmul_rn(kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e], r);
+                if (has_sc) z = __fmul_rn(z, __fadd_rn(1.0f, sc[e]));
+                if (has_sh) z = __fadd_rn(z, sh[e]);
+                y[e] = z;
+            }
+            v[i] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                              pack_bf16x2(y[6], y[7]));
+            if (np.y_out != nullptr)
+                *reinterpret_cast<uint4*>(np.y_out + out0 + static_cast<int64_t>(idx) * 8) = v[i];
+            IV::absmax(v[i], m2);
+        }
+    }
+    const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red_max);
+    const RowScale rs = row_scale(amax);
+    if (t == 0) S[row] = rs.s;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int idx = t + i * T;
+        if (idx < V) quantize_vector<__nv_bfloat16, kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+    }
+}
+
+}  // namespace w8a8

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda.h>
 
 namespace w8a8 {
@@ -75,6 +76,14 @@ __device__ __forceinline__ void grid_wait_prerequisites()
 }
 
 // ---------------------------------------------------------------- global visibility
+
+// Two floats rounded to bf16 (nearest, ties to even) in one instruction;
+// `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 // Orders this thread's generic-proxy global accesses with async-proxy (TMA,
 // bulk copy) accesses of the same memory, in both directions.

@@ -14,6 +14,7 @@
 #include "gemm_tcgen05.cuh"
 #include "quant_rows.cuh"
 #include "quant_blocks.cuh"
+#include "norm_quant.cuh"
 
 namespace {
 
@@ -536,6 +537,64 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[W8A8_NOALLOC_SCRATCH_
 void* g_noalloc_ptr[kMaxDevices] = {};
 std::mutex g_noalloc_mutex;
 
+// ---------------------------------------------------------------- norm + modulation + quant
+
+template <bool kBf16Codes, int NV, int kRows, int kNorm>
+void launch_norm_cfg(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormParams& np, void* Q, float* S,
+                     uint32_t* header, unsigned threads, cudaStream_t stream)
+{
+    const int64_t blocks = (M + kRows - 1) / kRows;
+    w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kNorm><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(X), M, K, np, Q, S, header);
+}
+
+// Rows of up to 128 vectors: a warp per row with 4 vectors per lane; up to
+// 512: 16 per lane; up to 4096 (K <= 32768): a CTA per row, 16 per thread.
+template <bool kBf16Codes, int kNorm>
+w8a8_status launch_norm_typed(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormParams& np, void* Q,
+                              float* S, uint32_t* header, cudaStream_t stream)
+{
+    const int64_t V = K / 8;
+    if (V <= 128)
+        launch_norm_cfg<kBf16Codes, 4, 4, kNorm>(X, M, K, np, Q, S, header, 128, stream);
+    else if (V <= 512)
+        launch_norm_cfg<kBf16Codes, 16, 4, kNorm>(X, M, K, np, Q, S, header, 128, stream);
+    else {
+        const unsigned T = static_cast<unsigned>(((V + 15) / 16 + 31) / 32 * 32);
+        launch_norm_cfg<kBf16Codes, 16, 1, kNorm>(X, M, K, np, Q, S, header, T, stream);
+    }
+    return last_launch_status();
+}
+
+template <bool kBf16Codes>
+w8a8_status launch_norm_quant(const uint16_t* X, int64_t M, int64_t K, int norm, const w8a8::NormParams& np,
+                              void* Q, float* S, uint32_t* header, cudaStream_t stream)
+{
+    if (norm == W8A8_NORM_RMS)
+        return launch_norm_typed<kBf16Codes, w8a8::kNormRms>(X, M, K, np, Q, S, header, stream);
+    return launch_norm_typed<kBf16Codes, w8a8::kNormLayer>(X, M, K, np, Q, S, header, stream);
+}
+
+// Host checks shared by the norm entry points (everything but the outputs).
+w8a8_status check_norm_args(const uint16_t* X, int64_t M, int64_t K, int norm, float eps, const void* scale,
+                            const void* shift, int mod_dtype, const void* y_mod, w8a8::NormParams* np)
+{
+    if (!X || M < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
+    if (norm != W8A8_NORM_RMS && norm != W8A8_NORM_LAYER) return W8A8_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !(eps <= 3.4e38f)) return W8A8_ERR_INVALID_ARG;
+    if ((scale || shift) && mod_dtype != W8A8_F32 && mod_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (M < 1 || M > INT32_MAX || K < 16 || K % 16 != 0 || K > W8A8_NORM_MAX_K) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(X, 16) || (scale && !aligned(scale, 16)) || (shift && !aligned(shift, 16)) ||
+        (y_mod && !aligned(y_mod, 16)))
+        return W8A8_ERR_ALIGNMENT;
+    np->eps = eps;
+    np->scale = scale;
+    np->shift = shift;
+    np->mod_f32 = mod_dtype == W8A8_F32 ? 1 : 0;
+    np->y_out = static_cast<uint16_t*>(const_cast<void*>(y_mod));
+    return W8A8_OK;
+}
+
 // ---------------------------------------------------------------- Query/Key blocks
 
 template <typename TIn, int NV>
@@ -907,6 +966,47 @@ w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64
     if (x_dtype == W8A8_BF16)
         return launch_blocks_typed<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(X), g, blocks, Xq, scales, s);
     return launch_blocks_typed<float>(static_cast<const float*>(X), g, blocks, Xq, scales, s);
+}
+
+w8a8_status w8a8_norm_quantize_act(const uint16_t* X, int64_t M, int64_t K, int norm, float eps, const void* scale,
+                                   const void* shift, int mod_dtype, uint16_t* Y_mod, int8_t* Xq, float* sx,
+                                   void* stream)
+{
+    if (M == 0 && X && K >= 0) return W8A8_OK;
+    w8a8::NormParams np;
+    w8a8_status st = check_norm_args(X, M, K, norm, eps, scale, shift, mod_dtype, Y_mod, &np);
+    if (st != W8A8_OK) return st;
+    if (!Xq || !sx) return W8A8_ERR_INVALID_ARG;
+    if (!aligned(Xq, 16) || !aligned(sx, 4)) return W8A8_ERR_ALIGNMENT;
+    if (!device_info(nullptr)) return W8A8_ERR_NO_DEVICE;
+    return launch_norm_quant<false>(X, M, K, norm, np, Xq, sx, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_norm_linear(const uint16_t* X, int64_t M, int64_t K, int norm, float eps, const void* scale,
+                             const void* shift, int mod_dtype, const uint16_t* Wp, const float* sw, int64_t N,
+                             const void* bias, int bias_dtype, uint16_t* Y, void* ws, size_t ws_bytes, void* stream)
+{
+    w8a8::NormParams np;
+    w8a8_status st = check_norm_args(X, M, K, norm, eps, scale, shift, mod_dtype, nullptr, &np);
+    if (st != W8A8_OK) return st;
+    if (!Wp || !sw || !Y || N < 0) return W8A8_ERR_INVALID_ARG;
+    if (bias && bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) return W8A8_ERR_DTYPE;
+    if (guard_reasons(M, N, K, W8A8_BF16, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    WsLayout L;
+    if (!ws || !ws_layout(M, K, &L) || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
+    if (!aligned(Wp, 16) || !aligned(Y, 16) || !aligned(ws, 16) || !aligned(sw, 16)) return W8A8_ERR_ALIGNMENT;
+    if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
+    int devno = 0;
+    DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(&devno));
+    if (!dev) return W8A8_ERR_NO_DEVICE;
+    uint8_t* w = ws_base(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = launch_norm_quant<true>(X, M, K, norm, np, w + L.codes_off, reinterpret_cast<float*>(w + L.sx_off),
+                                 reinterpret_cast<uint32_t*>(w + L.status_off), s);
+    if (st != W8A8_OK) return st;
+    return launch_gemm<w8a8::kModeW8A8>(dev, reinterpret_cast<const uint16_t*>(w + L.codes_off), Wp, M, N, K,
+                                        reinterpret_cast<const float*>(w + L.sx_off), sw, bias,
+                                        bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0, Y, w, L, ws_slots(L, ws_bytes), s);
 }
 
 size_t w8a8_mlp_workspace_bytes(int64_t M, int64_t K, int64_t F, int64_t N)
