@@ -20,7 +20,8 @@
 // Structure: as the quantiser (a warp per row, four rows per CTA, up to 16
 // vectors per lane, for K <= 4096; a CTA per row up to 32768), with the row
 // held in registers through three reductions: the sum (LayerNorm), the sum
-// of squared deviations, and the absmax of y.
+// of squared deviations, and the absmax of y.  In the warp form the CTA
+// prepares the modulation once in shared memory as fp32 (1 + scale, shift).
 #pragma once
 
 #include <cstdint>
@@ -112,7 +113,7 @@ __device__ __forceinline__ void keep_packed(uint4 (&v)[NV])
 }
 
 template <bool kBf16Codes, int NV, int kRowsPerCta, int kNorm>
-__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256)
+__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRowsPerCta > 1 ? 20 / kRowsPerCta : 1)
     norm_quant_rows_kernel(const __nv_bfloat16* __restrict__ A, int64_t R, int64_t K, NormParams np,
                            void* __restrict__ Q, float* __restrict__ S, uint32_t* __restrict__ header)
 {
@@ -122,6 +123,34 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256)
     grid_launch_dependents();
     if (header != nullptr && blockIdx.x == 0)
         for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
+
+    const bool has_sc = np.scale != nullptr, has_sh = np.shift != nullptr;
+    // Warp form: the CTA first turns the modulation into fp32 a = 1 + scale
+    // (1 without scale) and b = shift (-0 without shift, which leaves every
+    // sum unchanged) in shared memory, as four float4 arrays of V entries
+    // (elements 0-3 and 4-7 of each vector apart, so that lanes reading
+    // neighbouring vectors hit distinct banks).  y = (x r) a + b then takes
+    // the same roundings as the steps it stands for.
+    extern __shared__ float4 s_mod[];
+    const int Vall = static_cast<int>(K / 8);
+    if constexpr (kRowsPerCta > 1) {
+        for (int k8 = threadIdx.x; k8 < Vall; k8 += blockDim.x) {
+            float sc[8], sh[8];
+            if (has_sc) unpack_mod(load_mod(np.scale, np.mod_f32, k8), np.mod_f32, sc);
+            if (has_sh) unpack_mod(load_mod(np.shift, np.mod_f32, k8), np.mod_f32, sh);
+            float a[8], b[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                a[e] = has_sc ? __fadd_rn(1.0f, sc[e]) : 1.0f;
+                b[e] = has_sh ? sh[e] : -0.0f;
+            }
+            s_mod[k8] = make_float4(a[0], a[1], a[2], a[3]);
+            s_mod[Vall + k8] = make_float4(a[4], a[5], a[6], a[7]);
+            s_mod[2 * Vall + k8] = make_float4(b[0], b[1], b[2], b[3]);
+            s_mod[3 * Vall + k8] = make_float4(b[4], b[5], b[6], b[7]);
+        }
+        __syncthreads();
+    }
 
     const int64_t row = kRowsPerCta > 1 ? static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5)
                                         : static_cast<int64_t>(blockIdx.x);
@@ -138,13 +167,6 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256)
     for (int i = 0; i < NV; ++i) {
         const int idx = t + i * T;
         v[i] = (idx < V) ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
-    }
-    // The first modulation vectors, in flight during the reductions.
-    const bool has_sc = np.scale != nullptr, has_sh = np.shift != nullptr;
-    ModVec nsc = {}, nsh = {};
-    if (t < V) {
-        if (has_sc) nsc = load_mod(np.scale, np.mod_f32, t);
-        if (has_sh) nsh = load_mod(np.shift, np.mod_f32, t);
     }
 
     // Each sum runs in eight independent partial sums per thread (one per
@@ -183,31 +205,36 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256)
     keep_packed(v);
     const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(q, kf), np.eps));
 
-    // y, rounded to bf16, replaces x in the registers.  The modulation
-    // vectors of the next vector are fetched while this one is computed (the
-    // same K-vectors for every row, so they come from L1).
+    // y, rounded to bf16, replaces x in the registers.
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int idx = t + i * T;
         if (idx < V) {
-            const ModVec csc = nsc, csh = nsh;
-            if (i + 1 < NV && idx + T < V) {
-                if (has_sc) nsc = load_mod(np.scale, np.mod_f32, idx + T);
-                if (has_sh) nsh = load_mod(np.shift, np.mod_f32, idx + T);
-            }
-            float x[8], sc[8], sh[8];
+            float x[8], a[8], b[8];
             IV::unpack(v[i], x);
-            if (has_sc) unpack_mod(csc, np.mod_f32, sc);
-            if (has_sh) unpack_mod(csh, np.mod_f32, sh);
+            if constexpr (kRowsPerCta > 1) {
+                const float4 a0 = s_mod[idx], a1 = s_mod[V + idx];
+                const float4 b0 = s_mod[2 * V + idx], b1 = s_mod[3 * V + idx];
+                a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+                a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+                b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+                b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+            } else {
+                float sc[8], sh[8];
+                if (has_sc) unpack_mod(load_mod(np.scale, np.mod_f32, idx), np.mod_f32, sc);
+                if (has_sh) unpack_mod(load_mod(np.shift, np.mod_f32, idx), np.mod_f32, sh);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    a[e] = has_sc ? __fadd_rn(1.0f, sc[e]) : 1.0f;
+                    b[e] = has_sh ? sh[e] : -0.0f;
+                }
+            }
             float y[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float z = __fmul_rn(kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e], r);
-                if (has_sc) z = __fmul_rn(z, __fadd_rn(1.0f, sc[e]));
-                if (has_sh) z = __fadd_rn(z, sh[e]);
-                y[e] = z;
-            }
+            for (int e = 0; e < 8; ++e)
+                y[e] = __fadd_rn(__fmul_rn(__fmul_rn(kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e], r), a[e]),
+                                 b[e]);
             v[i] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                               pack_bf16x2(y[6], y[7]));
             if (np.y_out != nullptr)

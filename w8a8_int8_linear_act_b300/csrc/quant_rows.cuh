@@ -220,17 +220,22 @@ __device__ __forceinline__ void quantize_vector(const uint4& vec, const RowScale
 }
 
 // Rows of A [R][K] -> codes Q [R][K] and scales S [R].
-//   kRowsPerCta > 1: blockDim.x == 32 * kRowsPerCta, warp w takes row
+//   kRowsPerCta > 0: blockDim.x == 32 * kRowsPerCta, warp w takes row
 //                    blockIdx.x * kRowsPerCta + w (rows past R do nothing);
-//   kRowsPerCta == 1: the whole CTA takes row blockIdx.x.
+//                    registers are capped so that 21 warps fit on an SM;
+//   kRowsPerCta == 0: the whole CTA takes row blockIdx.x.
 // NV > 0: each thread keeps up to NV vectors of the row in registers (single
 // HBM read).  NV == 0: two passes over the row (for very long rows).
 // `header`, when not NULL, is the workspace header (status word and the
 // GEMM's split-tile counters), cleared by block 0 at the start of a call.
 // `zero_rows`, when not NULL, is a per-row word cleared with the row's scale
 // (the row absmax that the following GEMM gathers for the next layer).
+constexpr int kQuantWarpsPerSm = 21;
+
 template <typename TIn, bool kBf16Codes, int NV, int kRowsPerCta>
-__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ? 256 : 1024)) quant_rows_kernel(const TIn* __restrict__ A, int64_t R, int64_t K,
+__global__ void __launch_bounds__(kRowsPerCta > 0 ? 32 * kRowsPerCta : (NV > 0 ? 256 : 1024),
+                                  kRowsPerCta > 0 ? kQuantWarpsPerSm / (kRowsPerCta > 0 ? kRowsPerCta : 1) : 1)
+    quant_rows_kernel(const TIn* __restrict__ A, int64_t R, int64_t K,
                                                           void* __restrict__ Q, float* __restrict__ S,
                                                           uint32_t* __restrict__ header,
                                                           uint32_t* __restrict__ zero_rows)
@@ -245,11 +250,11 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ?
     if (header != nullptr && blockIdx.x == 0)
         for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
 
-    const int64_t row = kRowsPerCta > 1 ? static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5)
+    const int64_t row = kRowsPerCta > 0 ? static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5)
                                         : static_cast<int64_t>(blockIdx.x);
-    if (kRowsPerCta > 1 && row >= R) return;   // warp-uniform; no block-wide barrier follows
-    const int T = kRowsPerCta > 1 ? 32 : static_cast<int>(blockDim.x);
-    const int t = kRowsPerCta > 1 ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
+    if (kRowsPerCta > 0 && row >= R) return;   // warp-uniform; no block-wide barrier follows
+    const int T = kRowsPerCta > 0 ? 32 : static_cast<int>(blockDim.x);
+    const int t = kRowsPerCta > 0 ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
     const int V = static_cast<int>(K / E);  // 16-byte vectors in the row (K % 16 == 0)
     const uint4* src = reinterpret_cast<const uint4*>(A + row * K);
     const int64_t out0 = row * K;
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ?
         }
 #pragma unroll
         for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
-        const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
+        const float amax = kRowsPerCta > 0 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
         const RowScale rs = row_scale(amax);
         if (t == 0) {
             S[row] = rs.s;
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : (NV > 0 ?
         }
     } else {
         for (int idx = t; idx < V; idx += T) IV::absmax(load_stream(src + idx), m2);
-        const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
+        const float amax = kRowsPerCta > 0 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red);
         const RowScale rs = row_scale(amax);
         if (t == 0) {
             S[row] = rs.s;

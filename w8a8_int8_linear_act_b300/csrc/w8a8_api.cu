@@ -295,15 +295,18 @@ template <typename TIn, bool kBf16Codes, int NV, int kRows>
 void launch_quant_cfg(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header, unsigned threads,
                       cudaStream_t stream, uint32_t* zero_rows)
 {
-    const int64_t blocks = (R + kRows - 1) / kRows;
+    constexpr int64_t kPer = kRows > 0 ? kRows : 1;   // rows per CTA (0: the CTA-per-row form)
+    const int64_t blocks = (R + kPer - 1) / kPer;
     w8a8::quant_rows_kernel<TIn, kBf16Codes, NV, kRows>
         <<<static_cast<unsigned>(blocks), threads, 0, stream>>>(A, R, K, Q, S, header, zero_rows);
 }
 
-// Rows of up to 512 16-byte vectors: a warp per row, four rows per CTA, each
-// lane holding up to 16 vectors.  Up to 4096 vectors: a CTA per row of
-// ceil(V / 16) threads rounded to warps.  Longer: a CTA of 1024 threads per
-// row reading it twice.
+// Rows of up to 512 16-byte vectors: a warp per row, kQuantRows rows per
+// CTA, each lane holding up to 16 vectors.  Up to 4096 vectors: a CTA per
+// row of ceil(V / 16) threads rounded to warps.  Longer: a CTA of 1024
+// threads per row reading it twice.
+constexpr int kQuantRows = 4;
+
 template <typename TIn, bool kBf16Codes>
 w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header,
                                cudaStream_t stream, uint32_t* zero_rows)
@@ -311,20 +314,20 @@ w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, floa
     constexpr int E = w8a8::InVec<TIn>::kElems;
     const int64_t V = K / E;  // vectors per row
     if (V <= 32)
-        launch_quant_cfg<TIn, kBf16Codes, 1, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
+        launch_quant_cfg<TIn, kBf16Codes, 1, kQuantRows>(A, R, K, Q, S, header, 32 * kQuantRows, stream, zero_rows);
     else if (V <= 64)
-        launch_quant_cfg<TIn, kBf16Codes, 2, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
+        launch_quant_cfg<TIn, kBf16Codes, 2, kQuantRows>(A, R, K, Q, S, header, 32 * kQuantRows, stream, zero_rows);
     else if (V <= 128)
-        launch_quant_cfg<TIn, kBf16Codes, 4, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
+        launch_quant_cfg<TIn, kBf16Codes, 4, kQuantRows>(A, R, K, Q, S, header, 32 * kQuantRows, stream, zero_rows);
     else if (V <= 256)
-        launch_quant_cfg<TIn, kBf16Codes, 8, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
+        launch_quant_cfg<TIn, kBf16Codes, 8, kQuantRows>(A, R, K, Q, S, header, 32 * kQuantRows, stream, zero_rows);
     else if (V <= 512)
-        launch_quant_cfg<TIn, kBf16Codes, 16, 4>(A, R, K, Q, S, header, 128, stream, zero_rows);
+        launch_quant_cfg<TIn, kBf16Codes, 16, kQuantRows>(A, R, K, Q, S, header, 32 * kQuantRows, stream, zero_rows);
     else if (V <= 4096) {
         const unsigned T = static_cast<unsigned>(((V + 15) / 16 + 31) / 32 * 32);
-        launch_quant_cfg<TIn, kBf16Codes, 16, 1>(A, R, K, Q, S, header, T, stream, zero_rows);
+        launch_quant_cfg<TIn, kBf16Codes, 16, 0>(A, R, K, Q, S, header, T, stream, zero_rows);
     } else
-        launch_quant_cfg<TIn, kBf16Codes, 0, 1>(A, R, K, Q, S, header, 1024, stream, zero_rows);
+        launch_quant_cfg<TIn, kBf16Codes, 0, 0>(A, R, K, Q, S, header, 1024, stream, zero_rows);
     return last_launch_status();
 }
 
@@ -544,8 +547,12 @@ void launch_norm_cfg(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormPa
                      uint32_t* header, unsigned threads, cudaStream_t stream)
 {
     const int64_t blocks = (M + kRows - 1) / kRows;
-    w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kNorm><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(X), M, K, np, Q, S, header);
+    // The warp form stages the fp32 modulation in shared memory: 8 B per
+    // element of a row (32 KB at its largest, K = 4096).
+    const size_t smem = kRows > 1 ? static_cast<size_t>(K) * 8u : 0u;
+    w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kNorm>
+        <<<static_cast<unsigned>(blocks), threads, smem, stream>>>(reinterpret_cast<const __nv_bfloat16*>(X), M, K,
+                                                                   np, Q, S, header);
 }
 
 // Rows of up to 128 vectors: a warp per row with 4 vectors per lane; up to
