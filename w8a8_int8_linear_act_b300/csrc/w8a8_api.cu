@@ -604,6 +604,8 @@ w8a8_status check_norm_args(const uint16_t* X, int64_t M, int64_t K, int norm, f
 
 // ---------------------------------------------------------------- Query/Key blocks
 
+constexpr int kBlockThreads = 256;   // threads per CTA of the Query/Key block quantiser, at most
+
 template <typename TIn, int NV>
 void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
                        cudaStream_t stream)
@@ -952,7 +954,7 @@ w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64
     // Tokens per pass: as many as 256 threads cover (more warps per SM; a
     // form with up to 16 vectors per thread and fewer threads measured
     // slower at the video attention shape).
-    const int64_t cap = 256 / g.vd;
+    const int64_t cap = kBlockThreads / g.vd;
     g.tpp = static_cast<int32_t>(cap < g.block_tokens ? cap : g.block_tokens);
     if (layout == W8A8_LAYOUT_HND) {
         g.stride_t = D;
