@@ -626,6 +626,32 @@ def run_ours(args):
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
     e2e_step = max_over_ranks(statistics.mean(e2e_ms), world)
+    # The copy floor of that call: the same two transfers (pinned host X to
+    # the device, device Y to pinned host) run concurrently with no compute.
+    c_h2d, c_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    Yd_src = torch.empty_like(Y)
+
+    def copies():
+        c_h2d.wait_stream(stream)
+        c_d2h.wait_stream(stream)
+        with torch.cuda.stream(c_h2d):
+            Xe.copy_(Xh, non_blocking=True)
+        with torch.cuda.stream(c_d2h):
+            Yh.copy_(Yd_src, non_blocking=True)
+        stream.wait_stream(c_h2d)
+        stream.wait_stream(c_d2h)
+
+    copies()
+    torch.cuda.synchronize()
+    floor_ms = []
+    for _ in range(e2e_steps):
+        e0.record(stream)
+        copies()
+        e1.record(stream)
+        e1.synchronize()
+        floor_ms.append(e0.elapsed_time(e1))
+    copy_floor = statistics.mean(floor_ms)
+    del Yd_src
 
     ops = case.ops
     pk = peaks()
@@ -661,7 +687,10 @@ def run_ours(args):
                                "kernel": "quant_rows_kernel (bf16 codes)", "algorithmic_bytes": quant_bytes},
             "e2e": {"value": world * ops / (e2e_step * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
-                    "d2h_bytes_per_step": Yh.numel() * Yh.element_size()},
+                    "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_step,
+                    "copy_floor_ms": copy_floor, "frac_of_copy_floor": copy_floor / e2e_step,
+                    "note": "w8a8_linear_host, 768-row chunks: copies in, compute and copies out of different "
+                            "chunks overlap; copy_floor_ms = the same two transfers alone, concurrently"},
             "gpu_launches": launches,
             "graph": graph,
             "kernel_split_ms": {"quant": quant_ms, "gemm": gemm_ms,
