@@ -77,8 +77,8 @@ typedef enum {
 } w8a8_dtype;
 
 /* Reasons reported by w8a8_shape_supported (bitwise OR). */
-#define W8A8_REASON_M          0x01  /* M < 1 or M > 2^31 - 1 */
-#define W8A8_REASON_N          0x02  /* N < 8, N % 8 != 0 or N > 2^31 - 1 */
+#define W8A8_REASON_M          0x01  /* M < 1 or M > 2^30 */
+#define W8A8_REASON_N          0x02  /* N < 8, N % 8 != 0 or N > 2^30 */
 #define W8A8_REASON_K          0x04  /* K < 16 or K % 16 != 0 */
 #define W8A8_REASON_K_RANGE    0x08  /* K > 133144: K * 127^2 could leave INT32 */
 #define W8A8_REASON_X_DTYPE    0x10  /* activation dtype is not F32 or BF16 */
@@ -290,18 +290,19 @@ W8A8_API w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M
  * architectural role as well as by shape.  Same tcgen05 GEMM, with the bf16
  * operands loaded as they are and fp32 accumulation:
  *   Y[m][n] = bf16_rne(sum_k X[m][k] * W[n][k] + bias[n])
- * (the products are exact in fp32; the sum is accumulated in fp32 by the
- * tensor cores in K-chunks of 1024 and the chunks are added in fp32, so it
- * is within fp32 rounding of the exact sum, not bit-reproducible against
- * another summation order).
+ * (the products are exact in fp32; the tensor cores accumulate the sum in
+ * fp32 over each tile's K range, and a tile whose K range the schedule cuts
+ * into segments adds the segments' fp32 sums in segment order, so the
+ * result is within fp32 rounding of the exact sum and the same on every
+ * call, but not bit-identical to another summation order).
  *   X    [M][K] bf16                                    in
  *   W    [N][K] bf16                                    in
  *   bias [N] of `bias_dtype` (F32 or BF16), or NULL     in
  *   Y    [M][N] bf16                                    out
  *   ws   >= 2048 bytes; w8a8_bf16_linear_workspace_bytes(M, N, K) for full
  *        speed (adds the K-split partial tiles, as for w8a8_linear)
- * Shapes: M >= 1, N >= 8 with N % 8 == 0, K >= 8 with K % 8 == 0 (16-byte
- * rows for the tensor copies); no limit on K.  Others return
+ * Shapes: 1 <= M <= 2^30, 8 <= N <= 2^30 with N % 8 == 0, 8 <= K <= 2^30
+ * with K % 8 == 0 (16-byte rows for the tensor copies).  Others return
  * W8A8_ERR_UNSUPPORTED_SHAPE with nothing launched; w8a8_bf16_linear_supported
  * reports which (W8A8_REASON_* bits).
  * ------------------------------------------------------------------------- */
@@ -382,7 +383,7 @@ W8A8_API w8a8_status w8a8_mlp(const void* X, int x_dtype, int64_t M, int64_t K, 
  *   Xq     int8 codes, same shape and layout as X                       out
  *   scales [B][H][ceil(L / block_tokens)] fp32                         out
  * Needs D % 8 == 0 and D <= 2048 for BF16 (D % 4 == 0 and D <= 1024 for
- * F32), block_tokens >= 1; X and Xq 16-byte aligned.  Any of B, H, L == 0
+ * F32), block_tokens >= 1, L <= 2^31 - 1; X and Xq 16-byte aligned.  Any of B, H, L == 0
  * is a no-op returning W8A8_OK.  Errors: W8A8_ERR_INVALID_ARG (NULL
  * pointer, negative size, unknown layout), W8A8_ERR_DTYPE,
  * W8A8_ERR_UNSUPPORTED_SHAPE (D or block_tokens), W8A8_ERR_ALIGNMENT; nothing

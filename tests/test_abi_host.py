@@ -251,6 +251,7 @@ def test_qk_blocks_argument_errors(lib):
     assert f(p, w8.BF16, 1, 2, 8, 4096, 0, 64, p, p, null) == 4        # D > 2048
     assert f(p, w8.F32, 1, 2, 8, 2048, 0, 64, p, p, null) == 4         # fp32 D > 1024
     assert f(p, w8.BF16, 1, 2, 8, 64, 0, 0, p, p, null) == 4           # block_tokens 0
+    assert f(p, w8.BF16, 1, 1, 1 << 31, 64, 0, 64, p, p, null) == 4    # L past int32
     assert f(ctypes.c_void_p(0x10008), w8.BF16, 1, 2, 8, 64, 0, 64, p, p, null) == 3
 
 

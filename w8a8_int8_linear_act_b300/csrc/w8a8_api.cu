@@ -136,12 +136,16 @@ void bf16_ws_layout(WsLayout* L)
     L->min_total = kAlign + L->slots_off;
 }
 
+// Largest M, N (and the BF16 path's K) the GEMM takes: its tile and k-block
+// counts are formed as (dim + tile - 1) / tile in 32-bit arithmetic.
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
 int bf16_guard_reasons(int64_t M, int64_t N, int64_t K, int bias_dtype)
 {
     int r = 0;
-    if (M < 1 || M > INT32_MAX) r |= W8A8_REASON_M;
-    if (N < 8 || N % 8 != 0 || N > INT32_MAX) r |= W8A8_REASON_N;
-    if (K < 8 || K % 8 != 0 || K > INT32_MAX) r |= W8A8_REASON_K;
+    if (M < 1 || M > kMaxDim) r |= W8A8_REASON_M;
+    if (N < 8 || N % 8 != 0 || N > kMaxDim) r |= W8A8_REASON_N;
+    if (K < 8 || K % 8 != 0 || K > kMaxDim) r |= W8A8_REASON_K;
     if (bias_dtype != W8A8_F32 && bias_dtype != W8A8_BF16) r |= W8A8_REASON_BIAS_DTYPE;
     return r;
 }
@@ -275,8 +279,8 @@ GemmPlan current_plan(int64_t M, int64_t N, int64_t K, int64_t max_slots)
 int guard_reasons(int64_t M, int64_t N, int64_t K, int x_dtype, int bias_dtype)
 {
     int r = 0;
-    if (M < 1 || M > INT32_MAX) r |= W8A8_REASON_M;
-    if (N < 8 || N % 8 != 0 || N > INT32_MAX) r |= W8A8_REASON_N;
+    if (M < 1 || M > kMaxDim) r |= W8A8_REASON_M;
+    if (N < 8 || N % 8 != 0 || N > kMaxDim) r |= W8A8_REASON_N;
     if (K < 16 || K % 16 != 0) r |= W8A8_REASON_K;
     if (K > W8A8_MAX_K) r |= W8A8_REASON_K_RANGE;
     if (x_dtype != W8A8_F32 && x_dtype != W8A8_BF16) r |= W8A8_REASON_X_DTYPE;
@@ -707,7 +711,7 @@ size_t w8a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K)
 
 int w8a8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t max_slots, int64_t* plan)
 {
-    if (!plan || M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return 0;
+    if (!plan || M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
     const int64_t slots = max_slots < 0 ? INT64_MAX : max_slots;
     const GemmPlan g = num_sms > 0 ? choose_plan(M, N, K, num_sms, num_sms / 2, slots) : current_plan(M, N, K, slots);
     plan[0] = g.dp_tiles;
@@ -943,7 +947,7 @@ w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64
     if (B == 0 || H == 0 || L == 0) return W8A8_OK;
     if (!X || !Xq || !scales) return W8A8_ERR_INVALID_ARG;
     const int64_t E = x_dtype == W8A8_BF16 ? 8 : 4;
-    if (D < E || D % E != 0 || D / E > 256 || block_tokens < 1) return W8A8_ERR_UNSUPPORTED_SHAPE;
+    if (D < E || D % E != 0 || D / E > 256 || block_tokens < 1 || L > INT32_MAX) return W8A8_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(X, 16) || !aligned(Xq, 16) || !aligned(scales, 4)) return W8A8_ERR_ALIGNMENT;
     w8a8::BlockGeom g;
     g.H = H;
