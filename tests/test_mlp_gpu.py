@@ -62,6 +62,7 @@ def check(X, w, dev, rows=None, workspace=None):
 
 
 @pytest.mark.parametrize("M,K,F,N", [
+    (1, 256, 512, 128),      # one row
     (64, 256, 512, 128),
     (300, 256, 528, 264),    # ragged M, F and N tiles
     (129, 512, 1040, 136),   # one row past a 128-row tile: the single-CTA form for neither layer

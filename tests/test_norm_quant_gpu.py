@@ -105,12 +105,14 @@ def mod_vectors(K, seed, dtype):
     (100, 2048, "layer", None),
     (5, 32768, "rms", torch.float32),       # the largest K
     (33, 1040, "rms", torch.bfloat16),      # ragged vector count per lane
+    (3, 16, "layer", torch.float32),        # the smallest K: two vectors per row
 ])
 def test_norm_quant_shapes(cuda_device, M, K, kind, mod):
     g = torch.Generator().manual_seed(M + K)
     X = (torch.randn(M, K, generator=g) * 3 + 0.5).to(torch.bfloat16)
     sc, sh = mod_vectors(K, K, mod) if mod is not None else (None, None)
-    check(X, kind, 1e-6, sc, sh, cuda_device)
+    # a few elements in the band are a large fraction of a tiny tensor
+    check(X, kind, 1e-6, sc, sh, cuda_device, max_band=0.05 if M * K >= 4096 else 0.25)
 
 
 def test_norm_quant_video_rows(cuda_device):
