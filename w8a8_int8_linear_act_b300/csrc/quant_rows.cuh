@@ -119,7 +119,8 @@ __device__ __forceinline__ RowScale row_scale(float amax)
     return rs;
 }
 
-// Writes E codes given as integer-valued floats q, at element offset `off`.
+// Writes E codes at element offset `off`: for bf16 codes q holds the codes
+// as integer-valued floats, for int8 codes it holds kRoundMagic + code.
 template <bool kBf16Codes, int E>
 __device__ __forceinline__ void store_codes(void* Q, int64_t off, const float (&q)[E])
 {
@@ -135,11 +136,12 @@ __device__ __forceinline__ void store_codes(void* Q, int64_t off, const float (&
         else
             *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
     } else {
-        // The low byte of bits(kRoundMagic + q) is q's two's-complement byte
-        // (kRoundMagicBits has a zero low byte and |q| < 2^22).
+        // q here holds kRoundMagic + code (see quantize_vector): the low
+        // byte of its bits is the code's two's-complement byte
+        // (kRoundMagicBits has a zero low byte and |code| < 2^22).
         uint32_t b[E];
 #pragma unroll
-        for (int i = 0; i < E; ++i) b[i] = __float_as_uint(__fadd_rn(q[i], kRoundMagic));
+        for (int i = 0; i < E; ++i) b[i] = __float_as_uint(q[i]);
         uint32_t w[E / 4];
 #pragma unroll
         for (int i = 0; i < E / 4; ++i) {
@@ -204,19 +206,28 @@ __device__ __forceinline__ void quantize_vector(const uint4& vec, const RowScale
     constexpr int E = IV::kElems;
     float x[E];
     IV::unpack(vec, x);
-    float q[E];
+    // t = kRoundMagic + code; the int8 store takes t as it is, the bf16 one
+    // the code q = t - kRoundMagic.
+    float t[E], q[E];
     float dmax = 0.0f;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        q[e] = __fsub_rn(__fmaf_rn(x[e], rs.r, kRoundMagic), kRoundMagic);
+        t[e] = __fmaf_rn(x[e], rs.r, kRoundMagic);
+        q[e] = __fsub_rn(t[e], kRoundMagic);
         dmax = fmaxf(dmax, fabsf(__fmaf_rn(x[e], rs.r, -q[e])));
     }
     if (dmax > kNearHalf || rs.exact) {
 #pragma unroll
         for (int e = 0; e < E; ++e)
-            if (rs.exact || fabsf(__fmaf_rn(x[e], rs.r, -q[e])) > kNearHalf) q[e] = code_by_division(x[e], rs.s);
+            if (rs.exact || fabsf(__fmaf_rn(x[e], rs.r, -q[e])) > kNearHalf) {
+                q[e] = code_by_division(x[e], rs.s);
+                t[e] = __fadd_rn(q[e], kRoundMagic);
+            }
     }
-    store_codes<kBf16Codes, E>(Q, off, q);
+    if constexpr (kBf16Codes)
+        store_codes<true, E>(Q, off, q);
+    else
+        store_codes<false, E>(Q, off, t);
 }
 
 // Rows of A [R][K] -> codes Q [R][K] and scales S [R].
