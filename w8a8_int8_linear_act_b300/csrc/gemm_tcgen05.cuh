@@ -47,6 +47,14 @@
 // accumulator) and runs the epilogue, then resets the counter.  No CTA ever
 // waits for another CTA's segment.
 //
+// Other modes (kMode below): the INT32 sums themselves (a test entry point);
+// bf16 activations and weights with fp32 sums, the native BF16 linear (one
+// tensor-memory accumulation per unit, split partials added in segment
+// order); and the W8A8 epilogue that also gathers each row's max |Y| for
+// the next layer's activation scale (the MLP pair).  The kernel waits for
+// the kernel before it (programmatic dependent launch) only after its
+// set-up, and lets the kernel after it launch at the same point.
+//
 // Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
 // sets a bit in the status word and the CTA unwinds (waiting, again with a
 // limit, for its own copies and MMAs in flight) and frees its tensor memory.
