@@ -697,7 +697,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
                     "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_step,
                     "copy_floor_ms": copy_floor, "frac_of_copy_floor": copy_floor / e2e_step,
-                    "note": "w8a8_linear_host, 768-row chunks: copies in, compute and copies out of different "
+                    "note": "w8a8_linear_host, default chunks: copies in, compute and copies out of different "
                             "chunks overlap; copy_floor_ms = the same two transfers alone, concurrently"},
             "gpu_launches": launches,
             "graph": graph,

@@ -843,10 +843,21 @@ w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t
     if (guard_reasons(M, N, K, x_dtype, bias ? bias_dtype : W8A8_F32) != 0) return W8A8_ERR_UNSUPPORTED_SHAPE;
     // Row chunks: the copies of one chunk overlap the other chunks' compute
     // and copies in the other direction.  Default: about eight chunks of
-    // whole 256-row tiles.
+    // whole 256-row tiles, with the first and the last chunk a third of
+    // that (whole 128-row tiles): only the first chunk's copy in and the
+    // last chunk's compute and copy out run without the other direction's
+    // copies beside them.  A nonzero chunk_rows gives equal chunks.
     int64_t rows = chunk_rows;
-    if (rows == 0) rows = ((M + 7) / 8 + 255) / 256 * 256;
-    if ((M + rows - 1) / rows > kMaxHostChunks) rows = (M + kMaxHostChunks - 1) / kMaxHostChunks;
+    int64_t edge = 0;   // rows of the first and last chunk (0: equal chunks)
+    if (rows == 0) {
+        rows = ((M + 7) / 8 + 255) / 256 * 256;
+        edge = rows / 3 / 128 * 128;
+        if (edge < 128 || M <= rows + 2 * edge) edge = 0;
+    }
+    if ((M + rows - 1) / rows + 2 > kMaxHostChunks) {
+        rows = (M + kMaxHostChunks - 3) / (kMaxHostChunks - 2);
+        edge = 0;
+    }
     WsLayout L;
     if (!ws || !ws_layout(rows < M ? rows : M, K, &L) || ws_bytes < L.min_total) return W8A8_ERR_WORKSPACE;
     if (!aligned(X_dev, 16) || !aligned(Y_dev, 16) || !aligned(Wp, 16) || !aligned(sw, 16) || !aligned(ws, 16))
@@ -869,8 +880,14 @@ w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t
         return W8A8_ERR_CUDA;
     }
     int c = 0;
-    for (int64_t r0 = 0; r0 < M; r0 += rows, ++c) {
-        const int64_t mr = (M - r0) < rows ? (M - r0) : rows;
+    for (int64_t r0 = 0, mr = 0; r0 < M; r0 += mr, ++c) {
+        const int64_t left = M - r0;
+        if (edge > 0 && r0 == 0)
+            mr = edge;                                   // first chunk
+        else if (edge > 0 && left <= rows + edge && left > edge)
+            mr = left - edge;                            // the chunk before the last
+        else
+            mr = left < rows ? left : rows;              // middle chunks, and the last
         const uint8_t* xh = static_cast<const uint8_t*>(X_host) + static_cast<size_t>(r0) * x_row;
         uint8_t* xd = static_cast<uint8_t*>(X_dev) + static_cast<size_t>(r0) * x_row;
         uint16_t* yd = Y_dev + static_cast<size_t>(r0) * static_cast<size_t>(N);
