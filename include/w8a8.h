@@ -259,8 +259,9 @@ W8A8_API w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, 
  *   Y_dev  [M][N] bf16, device staging                       (caller-owned)
  *   ws     >= w8a8_linear_workspace_min_bytes(chunk, K) for the chunk size
  *          used (w8a8_linear_workspace_bytes(chunk, N, K) for full speed)
- *   chunk_rows  rows per chunk; 0 = about M / 8 rounded up to 256 rows (at
- *          most 64 chunks)
+ *   chunk_rows  rows per chunk (equal chunks, at most 64); 0 = about M / 8
+ *          rounded up to 256 rows, with the first and the last chunk a
+ *          third as long (whole 128-row tiles) when M is large enough
  * Wp, sw, bias as in w8a8_linear.  For each chunk of rows: the host-to-device
  * copy of X on a copy stream, then w8a8_linear on `stream`, then the
  * device-to-host copy of Y on a second copy stream, so the copies of one
