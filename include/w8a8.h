@@ -320,7 +320,7 @@ W8A8_API w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, c
  * reads and writes; arXiv paper, appendix C).  Per row x of X [M][K] bf16:
  *   mu = 0 (W8A8_NORM_RMS) or fp32(sum x / K) (W8A8_NORM_LAYER)
  *   r  = 1 / sqrt(fp32(sum (x - mu)^2 / K) + eps)   (correctly rounded)
- *   y  = bf16_rne(((x - mu) * r) * (1 + scale) + shift)   (fp32 steps)
+ *   y  = bf16_rne(fma((x - mu) * r, 1 + scale, shift))   (fp32 steps)
  * then y is quantised by the row rule (as w8a8_quantize_act).  scale and
  * shift are optional [K] vectors of `mod_dtype` (F32 or BF16, 16-byte
  * aligned), shared by all rows; NULL omits that step.  The fp32 sums run

@@ -9,9 +9,10 @@
 //   LayerNorm:  mu = fp32(sum_k x_k / K)
 //   v   = fp32(sum_k (x_k - mu)^2 / K)
 //   r   = 1 / sqrt(v + eps)                     (correctly rounded fp32)
-//   y_k = bf16_rne(((x_k - mu) * r) * (1 + scale_k) + shift_k)
+//   y_k = bf16_rne(fma((x_k - mu) * r, 1 + scale_k, shift_k))
 //
-// each step one fp32 operation rounded to nearest (the sums in any order);
+// each step one fp32 operation rounded to nearest, the last multiply and add
+// fused into one (the sums in any order);
 // scale and shift are optional [K] vectors (adaLN-style modulation shared by
 // all rows).  y is then quantised by the row rule of quant_rows.cuh, and
 // optionally also written out.  The unfused form would write y (2 B per
@@ -129,8 +130,9 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRow
     // (1 without scale) and b = shift (-0 without shift, which leaves every
     // sum unchanged) in shared memory, as four float4 arrays of V entries
     // (elements 0-3 and 4-7 of each vector apart, so that lanes reading
-    // neighbouring vectors hit distinct banks).  y = (x r) a + b then takes
-    // the same roundings as the steps it stands for.
+    // neighbouring vectors hit distinct banks).  fma(x r, 1, -0) and
+    // fma(x r, a, -0) equal x r and (x r) a exactly, so y = fma(x r, a, b)
+    // takes the same roundings as the steps it stands for.
     extern __shared__ float4 s_mod[];
     const int Vall = static_cast<int>(K / 8);
     if constexpr (kRowsPerCta > 1) {
@@ -233,8 +235,7 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRow
             float y[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                y[e] = __fadd_rn(__fmul_rn(__fmul_rn(kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e], r), a[e]),
-                                 b[e]);
+                y[e] = __fmaf_rn(__fmul_rn(kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e], r), a[e], b[e]);
             v[i] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                               pack_bf16x2(y[6], y[7]));
             if (np.y_out != nullptr)
