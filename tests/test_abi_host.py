@@ -30,8 +30,25 @@ def test_header_declares_the_api():
     names = declared_symbols()
     for required in ("w8a8_quantize_weight", "w8a8_quantize_act", "w8a8_linear", "w8a8_shape_supported",
                      "w8a8_pack_weight", "w8a8_gemm_s32", "w8a8_linear_workspace_bytes",
-                     "w8a8_linear_workspace_min_bytes", "w8a8_gemm_plan"):
+                     "w8a8_linear_workspace_min_bytes", "w8a8_gemm_plan", "w8a8_bf16_linear",
+                     "w8a8_bf16_linear_supported", "w8a8_mlp", "w8a8_norm_linear", "w8a8_norm_quantize_act",
+                     "w8a8_quantize_qk_blocks", "w8a8_linear_host", "w8a8_linear_noalloc"):
         assert required in names
+
+
+def test_header_is_plain_c(tmp_path):
+    """The boundary is a C ABI: the header compiles as C99 with no warnings."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text('#include "w8a8.h"\nint main(void) { return w8a8_version() > 0 ? 0 : 1; }\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I", inc, str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
 
 
 def test_library_exports_every_declared_symbol(lib):
