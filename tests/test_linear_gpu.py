@@ -234,3 +234,29 @@ def test_linear_repeated_calls_equal_stage_calls(cuda_device, case, M, N, K):
     torch.cuda.synchronize()
     for i, o in enumerate(outs):
         assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), "call %d differs" % i
+
+
+def test_linear_matches_the_golden_fixture(cuda_device):
+    """The CUDA path on tests/golden/linear_small.json (written by the
+    oracle): codes, scales and accumulators bit-exact, outputs within one
+    bf16 ulp (identical in practice)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "linear_small.json")
+    g = json.load(open(path))
+    as_bf16 = lambda a: torch.from_numpy(np.array(a, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    X, W, b = as_bf16(g["X_bf16_bits"]), as_bf16(g["W_bf16_bits"]), as_bf16(g["bias_bf16_bits"])
+    dev = cuda_device
+    Wq, sw = w8.quantize_weight(W.to(dev))
+    Xq, sx = w8.quantize_act(X.to(dev))
+    Wp = w8.pack_weight(Wq)
+    acc = w8.gemm_s32(Xq, Wp)
+    Y = w8.linear(X.to(dev), Wp, sw, b.to(dev))
+    torch.cuda.synchronize()
+    assert np.array_equal(Xq.cpu().numpy(), np.array(g["Xq"])) and np.array_equal(Wq.cpu().numpy(), np.array(g["Wq"]))
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), np.array(g["sx_f32_bits"], dtype=np.uint32))
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), np.array(g["sw_f32_bits"], dtype=np.uint32))
+    assert np.array_equal(acc.cpu().numpy(), np.array(g["acc"]))
+    want = oracle.bf16_bits_to_f32(np.array(g["Y_bf16_bits"], dtype=np.uint16)).astype(np.float64)
+    got = oracle.bf16_bits_to_f32(bits(Y)).astype(np.float64)
+    assert (np.abs(got - want) <= oracle.ulp_bf16(want)).all()

@@ -560,3 +560,25 @@ def test_bf16_rne_array_matches_scalar():
                         np.array([0.0, -0.0, 1.00390625, 1.01171875, np.inf, -np.inf, 3.4e38], dtype=np.float32)])
     lib = oracle._load()
     assert np.array_equal(oracle.bf16_rne(v), np.array([lib.oracle_bf16_rne(float(t)) for t in v], dtype=np.uint16))
+
+
+# ---------------------------------------------------------------- stored fixture
+
+def test_oracle_reproduces_the_golden_fixture():
+    """tests/golden/linear_small.json was written by the oracle
+    (make_golden.py); the oracle must still produce it bit for bit."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "linear_small.json")
+    g = json.load(open(path))
+    xb = np.array(g["X_bf16_bits"], dtype=np.uint16)
+    wb = np.array(g["W_bf16_bits"], dtype=np.uint16)
+    bb = np.array(g["bias_bf16_bits"], dtype=np.uint16)
+    wq, sw = oracle.quantize_rows(wb)
+    xq, sx = oracle.quantize_rows(xb)
+    assert np.array_equal(xq, np.array(g["Xq"])) and np.array_equal(wq, np.array(g["Wq"]))
+    assert np.array_equal(sx.view(np.uint32), np.array(g["sx_f32_bits"], dtype=np.uint32))
+    assert np.array_equal(sw.view(np.uint32), np.array(g["sw_f32_bits"], dtype=np.uint32))
+    assert np.array_equal(oracle.gemm_s32(xq, wq, np.arange(xq.shape[0])), np.array(g["acc"]))
+    ref = oracle.linear(xb, wq, sw, oracle.bf16_bits_to_f32(bb))
+    assert np.array_equal(ref["y"], np.array(g["Y_bf16_bits"], dtype=np.uint16))
