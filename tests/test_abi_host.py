@@ -313,3 +313,32 @@ def test_norm_argument_errors(lib):
     g = lib.w8a8_norm_linear
     assert g(p, 4, 64, 1, 1e-6, null, null, 1, p, p, 12, null, 1, p, p, 1 << 20, null) == 4
     assert g(p, 4, 64, 1, 1e-6, null, null, 1, p, p, 128, null, 1, p, p, 64, null) == 5
+
+
+def test_c_client_links_and_agrees_with_the_binding(tmp_path):
+    """A C program built against include/w8a8.h and libw8a8.so alone sees the
+    same guard, plan and workspace sizes as the Python binding."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    inc = os.path.join(os.path.dirname(here), "include")
+    libdir = os.path.dirname(w8.lib_path())
+    exe = tmp_path / "host_client"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", inc, os.path.join(here, "c_abi", "host_client.c"),
+                        "-L", libdir, "-l:libw8a8.so", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    lines = dict(line.split(" ", 1) for line in out.stdout.strip().splitlines())
+    assert lines["version"] == "1"
+    assert lines["guard"].split()[:2] == ["1", "0"]
+    assert tuple(int(v) for v in lines["plan"].split()[1:]) == w8.gemm_plan(6144, 4096, 4096, num_sms=148)
+    assert [int(v) for v in lines["workspace"].split()] == [w8.workspace_min_bytes(6144, 4096),
+                                                            w8.workspace_bytes(6144, 4096, 4096)]
+    assert int(lines["bf16"].split()[2]) == w8.bf16_linear_workspace_bytes(64, 128, 1032)
+    assert int(lines["mlp"]) == w8.mlp_workspace_bytes(6144, 4096, 16384, 4096)
+    assert lines["errors"] == "1 1"
