@@ -158,9 +158,10 @@ W8A8_API size_t w8a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* How the GEMM deals its output tiles to the device's SMs, for a workspace
  * with room for `max_slots` partial tiles of 128 x 256 INT32 (< 0:
- * unlimited).  For M > 128 a tile is 256 x 256 and runs on a pair of CTAs
- * on two SMs (one tcgen05 MMA of cta_group::2 for both); otherwise a tile is
- * 128 x 256 on one CTA.  `num_sms` > 0 plans for that many SMs (pairs:
+ * unlimited).  A tile is 256 x 256 and runs on a pair of CTAs on two SMs
+ * (one tcgen05 MMA of cta_group::2 for both), for any M; where pairs cannot
+ * be resident, or under w8a8_debug_force_single_cta, a tile is 128 x 256 on
+ * one CTA.  `num_sms` > 0 plans for that many SMs (pairs:
  * num_sms / 2); <= 0 plans for the current device as the launch will (148
  * SMs when none is current).  Writes plan[0] = whole tiles (dealt
  * round-robin to the workers), plan[1] = K-segments per remaining tile (1 =

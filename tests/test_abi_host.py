@@ -110,7 +110,7 @@ def test_workspace_min_bytes(lib):
 
 
 @pytest.mark.parametrize("M,N,K,plan", [
-    # M > 128: 256 x 256 tiles on CTA pairs (74 pairs on 148 SMs).
+    # 256 x 256 tiles on CTA pairs (74 pairs on 148 SMs), whatever M.
     # 384 tiles: 5 full waves, the 14 tiles left are cut in 5 (<= sqrt(64) k-blocks)
     (6144, 4096, 4096, (370, 5, 70, 148, 2)),
     (6144, 4096, 16384, (370, 5, 70, 148, 2)),
@@ -120,12 +120,12 @@ def test_workspace_min_bytes(lib):
     (1001, 2048, 2048, (32, 1, 0, 64, 2)),             # 32 k-blocks: tiles this short are never cut
     (1001, 8192, 2048, (128, 1, 0, 148, 2)),           # 128 tiles: 54 left > 37
     (256 * 37, 512, 4096, (74, 1, 0, 148, 2)),         # exactly one wave
-    # M <= 128: 128 x 256 tiles on single CTAs.
-    (126, 2048, 2048, (8, 1, 0, 8, 1)),                # 8 tiles of 32 k-blocks: too short to cut
-    (126, 8192, 2048, (32, 1, 0, 32, 1)),
-    (64, 128, 256, (1, 1, 0, 1, 1)),
-    (126, 2048, 4096, (0, 8, 64, 64, 1)),              # 64 k-blocks: cut in sqrt(64) = 8
-    (128, 256, 133136, (0, 45, 45, 45, 1)),            # 2081 k-blocks: sqrt caps at 45
+    # M <= 128 too: the odd CTA of each pair holds rows past M.
+    (126, 2048, 2048, (8, 1, 0, 16, 2)),               # 8 tiles of 32 k-blocks: too short to cut
+    (126, 8192, 2048, (32, 1, 0, 64, 2)),
+    (64, 128, 256, (1, 1, 0, 2, 2)),
+    (126, 2048, 4096, (0, 8, 64, 128, 2)),             # 64 k-blocks: cut in sqrt(64) = 8
+    (128, 256, 133136, (0, 45, 45, 90, 2)),            # 2081 k-blocks: sqrt caps at 45
 ])
 def test_gemm_plan_for_workload_shapes(lib, M, N, K, plan):
     assert w8.gemm_plan(M, N, K, num_sms=148) == plan
@@ -148,19 +148,20 @@ def test_gemm_plan_respects_workspace_room(lib):
     assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=100) == (370, 3, 42, 148, 2)
     assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=55) == (384, 1, 0, 148, 2)
     assert w8.gemm_plan(6144, 4096, 4096, 148, max_slots=0) == (384, 1, 0, 148, 2)
-    assert w8.gemm_plan(126, 2048, 4096, 148, max_slots=16) == (0, 2, 16, 16, 1)
+    assert w8.gemm_plan(126, 2048, 4096, 148, max_slots=16) == (8, 1, 0, 16, 2)   # 16 slots: 8 pair units
+    assert w8.gemm_plan(126, 2048, 4096, 148, max_slots=32) == (0, 2, 16, 32, 2)
 
 
 def test_gemm_plan_invariants(lib):
     """Every tile is either whole or cut into `splits` segments of >= 2
     k-blocks; the segment units fit the workers; no more than half a wave is
-    cut; CTA pairs exactly when M > 128."""
+    cut; CTA pairs whenever the device can hold them."""
     for sms in (148, 132, 8):
         for M in (1, 127, 128, 129, 1000, 6144, 28672):
             for N in (8, 256, 264, 2048, 4096, 16384):
                 for K in (16, 64, 128, 1024, 4096, 16384):
                     dp, s, units, grid, pair = w8.gemm_plan(M, N, K, sms)
-                    assert pair == (2 if M > 128 else 1)
+                    assert pair == 2
                     workers = sms // pair
                     tiles = -(-M // (128 * pair)) * -(-N // 256)
                     kb = -(-K // 64)

@@ -13,14 +13,21 @@ import w8a8_workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("M", [128, 256])    # single-CTA form, CTA-pair form
-def test_bounded_wait_reports_timeout_and_context_survives(cuda_device, M):
+@pytest.fixture(params=[True, False], ids=["single-CTA form", "CTA-pair form"])
+def single_cta(request):
+    w8.debug_force_single_cta(request.param)
+    yield request.param
+    w8.debug_force_single_cta(False)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(cuda_device, single_cta):
     dev = cuda_device
+    M = 256
     X, W, b = wl.make("video", M=M, N=512, K=512)
     Xd, bd = X.to(dev), b.to(dev)
     Wq, sw = w8.quantize_weight(W.to(dev))
     Wp = w8.pack_weight(Wq)
-    assert w8.gemm_plan(M, 512, 512)[4] == (1 if M == 128 else 2)
+    assert w8.gemm_plan(M, 512, 512)[4] == (1 if single_cta else 2)
     ws = torch.empty(w8.workspace_bytes(M, 512, 512), dtype=torch.uint8, device=dev)
     good = w8.linear(Xd, Wp, sw, bd, workspace=ws)
     assert w8.read_status(ws) == (0, 0)

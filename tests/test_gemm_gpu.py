@@ -138,6 +138,9 @@ def test_s32_k_split_and_whole_tiles_agree(cuda_device, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [
+    (1, 8, 16),           # one row: the pair's second CTA holds no row of X or Y
+    (126, 2048, 2048),    # the audio rows, all inside the first CTA of each pair
+    (64, 264, 1040),
     (129, 264, 2064),     # one row past a pair's first CTA: the second CTA's rows are all ragged
     (300, 520, 1040),
     (1000, 2048, 3200),

@@ -210,7 +210,7 @@ def test_linear_pair_and_single_cta_forms_identical(cuda_device):
 @pytest.mark.parametrize("case,M,N,K", [
     ("video", 1000, 520, 1024),         # ragged tiles, CTA pairs
     ("video", 6144, 4096, 4096),        # the benchmark's layer
-    ("tiny", 64, 128, 256),             # fp32 activations, single-CTA form
+    ("tiny", 64, 128, 256),             # fp32 activations, one 256-row pair tile for 64 rows
     ("audio_m126_n2048", 126, 2048, 2048),
     ("audio_m1001_n8192", 1001, 8192, 2048),
 ])
