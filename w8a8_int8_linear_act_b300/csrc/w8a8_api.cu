@@ -163,9 +163,10 @@ uint8_t* ws_base(const void* ws)
 
 // How the GEMM deals its output tiles to its workers (see gemm_tcgen05.cuh).
 // A worker is a CTA pair on two SMs (256-row tiles) or, where pairs cannot
-// be resident or the single-CTA test switch is on, one CTA (128-row tiles).  Full waves run whole tiles.  When the last wave
-// would be at most half full, its `rem` tiles are cut along K into `splits`
-// segments so that all workers share that wave.  The last segment of a tile
+// be resident or the single-CTA test switch is on, one CTA (128-row tiles).
+// Full waves run whole tiles.  When the last wave would be at most half
+// full, its `rem` tiles are cut along K into `splits` segments so that all
+// workers share that wave.  The last segment of a tile
 // to finish adds the other partials (each one 128 x 256 INT32 block read
 // from L2), so more segments cost more fix-up: splits stays near
 // sqrt(k-blocks), which balances the segment's MMA time (k-blocks / splits)
