@@ -2,13 +2,28 @@
 
 Metric: W8A8 linear TOPS (activation quantisation + INT32-exact GEMM + fused
 epilogue) on the video-branch projection, M=6144, K=N=4096, bf16 inputs with
-1 % outlier columns, on one GPU.  One step = one call of the whole hot path:
-the activation-quantisation kernel and the GEMM+epilogue kernel, through the
-C ABI's two stages (exactly what w8a8_linear runs), inputs resident in HBM,
-L2 flushed (256 MiB written) before every step, each kernel timed with CUDA
-events on the launching stream.
+1 % outlier columns, on one GPU.  One step = one call of w8a8_linear through
+the C ABI: the activation-quantisation kernel, then the GEMM+epilogue kernel
+as its programmatic dependent.  Inputs are resident in HBM, and L2 is flushed
+(256 MiB written) before every step.  Each step is timed with CUDA events on
+the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline] [--no-per-workload]
+
+The JSON line also carries:
+  int8_peak     the measured rates of every exact INT8 route on this GPU
+                (warp-level mma.sync s8, torch._int_mm, and the bf16 tcgen05
+                pipe that carries the codes here) and ptxas's answer on the
+                integer tcgen05 MMA; the largest rate is the denominator of
+                the metric's "% of INT8 tensor peak" (frac_of_int8_peak)
+  per_workload  every workload (tiny, video, MLP up and down, high-res x2,
+                audio x4): median step time of 50 cold-L2 steps and of 250
+                hot-L2 steps (graph replays), the quantiser and the GEMM
+                alone, the native BF16 linear on the same shape, and their
+                rooflines
+  roofline, quant_roofline, e2e, cpu_baseline, clocks, and the timings of
+                the MLP pair, the norm prologue and the Query/Key blocks
 
 --impl reference times the CPU oracle (plain C) on the host cores on a
 bounded row sample of the same workload.  Under torchrun (N > 1) every rank
@@ -16,6 +31,7 @@ runs an independent replica of the workload (rows are independent, no
 collective on the data path; "weak" scaling), rank 0 prints the line.
 """
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -35,10 +51,23 @@ METRIC = "W8A8 linear TOPS (quant+GEMM+epilogue) at M=6144,K=N=4096; % INT8 tens
 UNIT = "TOPS"
 WORKLOAD = "video"
 FLUSH_BYTES = 256 << 20
+PER_WORKLOAD_COLD = 50        # cold-L2 steps per per-workload measurement
+PER_WORKLOAD_GRAPH = 50       # steps per captured graph (hot L2)
+PER_WORKLOAD_REPLAYS = 5      # graph replays per hot-L2 measurement
 
-# Algorithmic bytes per unit, for the rooflines:
-#   quant kernel per activation element: 2 B read (bf16; 4 B for fp32) + 2 B written (bf16 code); + 4 B per row (scale)
-#   GEMM per launch: codes A (2 M K) + codes B (2 N K) + sx (4 M) + sw (4 N) + bias (2 N) + Y (2 M N)
+# Algorithmic bytes (the method's, SURVEY-style accounting with INT8 codes):
+#   quantiser per activation element: input (2 B bf16, 4 B fp32) + 1 B int8 code; + 4 B per row (scale)
+#   GEMM per launch: Xq (M K) + Wq (N K) + sx (4 M) + sw (4 N) + bias (2 N or 4 N) + Y (2 M N)
+# Bytes as built (the codes are carried as bf16 for the tensor cores):
+#   quantiser: input + 2 B per code + 4 B per row; GEMM: 2 B per code of Xq and Wq
+
+
+def quant_bytes(M, K, in_size, code_size=1):
+    return M * K * in_size + M * K * code_size + 4 * M
+
+
+def gemm_bytes(M, N, K, bias_size=2, code_size=1):
+    return code_size * (M * K + N * K) + 4 * M + 4 * N + bias_size * N + 2 * M * N
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM launch
@@ -78,11 +107,58 @@ def peaks():
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-class ClockSampler:
-    """Samples the SM clock and the clock-event (throttle) reasons while the
-    timed region runs (read-only queries).  NVML first, every 5 ms; if NVML
-    cannot be opened, `nvidia-smi --query-gpu ... -lms 50` in a child process."""
+# ---------------------------------------------------------------------------
+# SM clock and throttle reasons (read-only queries)
+# ---------------------------------------------------------------------------
 
+class _NvmlCtypes:
+    """The few read-only NVML queries the sampler needs, through ctypes on
+    the driver's libnvidia-ml (used when the Python NVML module is absent)."""
+
+    # nvmlClocksEventReason* bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, index, pci):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        rc = -1
+        if pci:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError("no NVML handle")
+        try:
+            self._reasons = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_clock(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(v)) == 0 else None
+
+    def max_sm_clock(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(v)) == 0 else None
+
+    def power_w(self):
+        v = ctypes.c_uint()
+        return v.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(v)) == 0 else None
+
+    def reasons(self):
+        v = ctypes.c_ulonglong()
+        if self._reasons(self.h, ctypes.byref(v)) != 0:
+            return set()
+        return {k for k, b in self.BITS.items() if v.value & b}
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+class _NvmlModule:
     REASONS = {
         "hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
         "hw_thermal_slowdown": "nvmlClocksEventReasonHwThermalSlowdown",
@@ -90,7 +166,41 @@ class ClockSampler:
         "sw_power_cap": "nvmlClocksEventReasonSwPowerCap",
         "hw_power_brake_slowdown": "nvmlClocksEventReasonHwPowerBrakeSlowdown",
     }
-    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+
+    def __init__(self, index, pci):
+        import pynvml
+        pynvml.nvmlInit()
+        self.nv = pynvml
+        self.h = (pynvml.nvmlDeviceGetHandleByPciBusId(pci.encode()) if pci
+                  else pynvml.nvmlDeviceGetHandleByIndex(index))
+        self.masks = {k: getattr(pynvml, v) for k, v in self.REASONS.items() if hasattr(pynvml, v)}
+
+    def sm_clock(self):
+        return self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+
+    def max_sm_clock(self):
+        return self.nv.nvmlDeviceGetMaxClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+
+    def power_w(self):
+        return self.nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+
+    def reasons(self):
+        active = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        return {k for k, m in self.masks.items() if active & m}
+
+    def close(self):
+        self.nv.nvmlShutdown()
+
+
+class ClockSampler:
+    """Samples the SM clock, power and the clock-event (throttle) reasons every
+    5 ms from before the first GPU work to after the last (read-only NVML
+    queries: the Python module, else ctypes on libnvidia-ml, else
+    `nvidia-smi -lms 20`).  `mark(name)` / `end(name)` bracket a region (the
+    headline's timed steps); `summary()` reports the whole run and each
+    region."""
+
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
                   "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
                   "clocks_event_reasons.sw_power_cap"]
 
@@ -98,61 +208,53 @@ class ClockSampler:
         self.index = index
         self.pci = pci_bus_id
         self.period = period_s
-        self.samples = []
-        self.reasons = set()
+        self.samples = []          # (t, sm_mhz, power_w, reasons)
         self.max_mhz = None
         self.source = None
-        self.error = None
+        self.errors = []
+        self.regions = {}
         self._stop = threading.Event()
         self._thread = None
-        self._nvml = None
+        self._q = None
         self._proc = None
 
     def __enter__(self):
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nvml = pynvml
-            if self.pci:
-                self._h = pynvml.nvmlDeviceGetHandleByPciBusId(self.pci.encode() if isinstance(self.pci, str)
-                                                              else self.pci)
-            else:
-                self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.source = "nvml"
-            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
-            self._thread.start()
-        except Exception as e:  # fall back to nvidia-smi
-            self.error = "nvml: %s: %s" % (type(e).__name__, e)
-            self._nvml = None
-            self._start_smi()
+        for cls, name in ((_NvmlModule, "nvml"), (_NvmlCtypes, "nvml-ctypes")):
+            try:
+                self._q = cls(self.index, self.pci)
+                self.max_mhz = self._q.max_sm_clock()
+                self.source = name
+                self._thread = threading.Thread(target=self._run_nvml, daemon=True)
+                self._thread.start()
+                return self
+            except Exception as e:  # try the next source
+                self.errors.append("%s: %s: %s" % (name, type(e).__name__, e))
+                self._q = None
+        self._start_smi()
         return self
 
     def _start_smi(self):
         import subprocess
         target = self.pci if self.pci else str(self.index)
         cmd = ["nvidia-smi", "-i", target, "--query-gpu=" + ",".join(self.SMI_FIELDS),
-               "--format=csv,noheader,nounits", "-lms", "50"]
+               "--format=csv,noheader,nounits", "-lms", "20"]
         try:
             self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.source = "nvidia-smi"
             self._thread = threading.Thread(target=self._run_smi, daemon=True)
             self._thread.start()
         except Exception as e:
-            self.error = (self.error or "") + "; nvidia-smi: %s" % e
+            self.errors.append("nvidia-smi: %s" % e)
 
     def _run_nvml(self):
-        nv = self._nvml
-        masks = {k: getattr(nv, v) for k, v in self.REASONS.items() if hasattr(nv, v)}
+        q = self._q
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                active = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                for name, m in masks.items():
-                    if active & m:
-                        self.reasons.add(name)
+                self.samples.append((time.perf_counter(), q.sm_clock(), q.power_w(), q.reasons()))
             except Exception as e:
-                self.error = "nvml sample: %s" % e
+                self.errors.append("sample: %s" % e)
+                if len(self.errors) > 20:
+                    return
             time.sleep(self.period)
 
     def _run_smi(self):
@@ -162,13 +264,18 @@ class ClockSampler:
             if len(parts) != len(self.SMI_FIELDS):
                 continue
             try:
-                self.samples.append(float(parts[0]))
-                self.max_mhz = float(parts[1])
+                mhz, self.max_mhz = float(parts[0]), float(parts[1])
+                pw = float(parts[2])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[2:]):
-                if val.lower() == "active":
-                    self.reasons.add(name)
+            reasons = {n for n, v in zip(names, parts[3:]) if v.lower() == "active"}
+            self.samples.append((time.perf_counter(), mhz, pw, reasons))
+
+    def mark(self, name):
+        self.regions[name] = [time.perf_counter(), None]
+
+    def end(self, name):
+        self.regions[name][1] = time.perf_counter()
 
     def __exit__(self, *exc):
         self._stop.set()
@@ -180,21 +287,42 @@ class ClockSampler:
                 self._proc.kill()
         if self._thread is not None:
             self._thread.join(timeout=5)
-        if self._nvml is not None:
+        if self._q is not None:
             try:
-                self._nvml.nvmlShutdown()
+                self._q.close()
             except Exception:
                 pass
         return False
 
+    @staticmethod
+    def _stats(samples, max_mhz):
+        if not samples:
+            return {"sm_mhz": None, "samples": 0, "reasons": ["unsampled"]}
+        # Samples under load: power above the run's idle level (the lowest
+        # tenth of the power readings plus 100 W), or all when power is unknown.
+        pw = sorted(p for _, _, p, _ in samples if p is not None)
+        idle = pw[len(pw) // 10] if pw else None
+        load = [s for s in samples if idle is None or s[2] is None or s[2] > idle + 100.0] or samples
+        reasons = set()
+        for s in load:
+            reasons |= s[3]
+        return {"sm_mhz": statistics.median(s[1] for s in load if s[1] is not None),
+                "sm_mhz_min": min(s[1] for s in load if s[1] is not None),
+                "sm_max_mhz": max_mhz, "reasons": sorted(reasons), "samples": len(samples),
+                "samples_under_load": len(load),
+                "power_w_max": max(pw) if pw else None}
+
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0,
-                    "source": self.source, "error": self.error}
-        out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-               "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.source}
-        if self.error:
-            out["error"] = self.error
+        out = self._stats(self.samples, self.max_mhz)
+        out["source"] = self.source
+        out["scope"] = "every 5 ms from before the warm-up to after the last GPU pass of this run"
+        for name, (t0, t1) in self.regions.items():
+            inside = [s for s in self.samples if t0 <= s[0] <= (t1 if t1 is not None else float("inf"))]
+            st = self._stats(inside, self.max_mhz)
+            st["seconds"] = (t1 - t0) if t1 is not None else None
+            out["region_" + name] = st
+        if self.errors:
+            out["errors"] = self.errors[:3]
         return out
 
 
@@ -257,7 +385,7 @@ def oracle_inputs(case, X, W, b):
 
 def calibrate_rows(case, inputs, target_s: float) -> int:
     rows = 8
-    dt, _ = oracle_sample(case, rows, *inputs)
+    dt, _ = oracle_sample(case, min(rows, case.M), *inputs)
     while dt < target_s / 8 and rows < case.M:
         rows = min(case.M, rows * 4)
         dt, _ = oracle_sample(case, rows, *inputs)
@@ -332,6 +460,236 @@ def config_dict(case):
 
 
 # ---------------------------------------------------------------------------
+# GPU timing helpers
+# ---------------------------------------------------------------------------
+
+class Timer:
+    """CUDA-event timing on one stream.  cold(): the 256 MiB flush before
+    every call, events around the call alone.  hot(): `per_graph` calls
+    captured back to back in one CUDA graph and replayed (no host work
+    between calls, L2 warm from the previous call); returns per-call times
+    of each replay."""
+
+    def __init__(self, stream, flush):
+        self.stream = stream
+        self.flush = flush
+        self.graphs = []      # captured graphs stay alive with the buffers they use, until release()
+
+    def cold(self, fn, n, warm=3):
+        for _ in range(warm):
+            self.flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            self.flush.zero_()
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def cold_split(self, fns, n, warm=3):
+        """Each of `fns` in turn after one flush, an event between them:
+        per-function times of each call."""
+        for _ in range(warm):
+            self.flush.zero_()
+            for f in fns:
+                f()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(n)]
+        for e in evs:
+            self.flush.zero_()
+            e[0].record(self.stream)
+            for i, f in enumerate(fns):
+                f()
+                e[i + 1].record(self.stream)
+        torch.cuda.synchronize()
+        return [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(len(fns))]
+
+    def hot(self, fn, per_graph=PER_WORKLOAD_GRAPH, replays=PER_WORKLOAD_REPLAYS):
+        g = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(self.stream)
+        with torch.cuda.stream(gs):
+            fn()
+            gs.synchronize()
+            with torch.cuda.graph(g, stream=gs):
+                for _ in range(per_graph):
+                    fn()
+        torch.cuda.synchronize()
+        self.graphs.append(g)
+        cur = torch.cuda.current_stream()
+        g.replay()
+        torch.cuda.synchronize()
+        out = []
+        for _ in range(replays):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            g.replay()
+            b.record(cur)
+            b.synchronize()
+            out.append(a.elapsed_time(b) / per_graph)
+        return out
+
+    def release(self):
+        torch.cuda.synchronize()
+        self.graphs = []
+
+
+def med(xs):
+    return statistics.median(xs)
+
+
+def int8_peaks(dev, pk):
+    """Rates of every exact INT8 x INT8 -> INT32 route this GPU offers, and
+    the denominator of the metric's "% of INT8 tensor peak": the largest."""
+    from w8a8_int8_linear_act_b300 import peaks as pp
+    out = {"unit": "TOPS"}
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, threads = 4 * sms, 256
+    sink = torch.zeros(blocks * threads, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def probe(kind):
+        iters = 256
+        pp.mma_sync_launch(kind, blocks, threads, iters, sink, stream)
+        torch.cuda.synchronize()
+        best = 0.0
+        for _ in range(2):                      # calibrate to about 40 ms per launch
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pp.mma_sync_launch(kind, blocks, threads, iters, sink, stream)
+            b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = max(best, pp.mma_sync_ops(kind, blocks, threads, iters) / (ms * 1e-3) / 1e12)
+            iters = int(min(1 << 22, max(iters, iters * 40.0 / max(ms, 1e-3))))
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pp.mma_sync_launch(kind, blocks, threads, iters, sink, stream)
+            b.record(stream)
+            b.synchronize()
+            best = max(best, pp.mma_sync_ops(kind, blocks, threads, iters) / (a.elapsed_time(b) * 1e-3) / 1e12)
+        return best
+
+    try:
+        out["mma_sync_s8"] = probe(pp.MMA_S8)
+        out["mma_sync_bf16_tflops"] = probe(pp.MMA_BF16)
+        out["mma_sync_note"] = ("warp-level mma.sync (m16n8k32 s8 / m16n8k16 bf16) from registers, %d CTAs x 8 "
+                                "warps x 8 independent MMAs, best of 3 launches of about 40 ms" % blocks)
+    except Exception as e:
+        out["mma_sync_error"] = "%s: %s" % (type(e).__name__, e)
+    try:
+        n = 8192
+        g = torch.Generator(device=dev).manual_seed(5)
+        A = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev, generator=g)
+        B = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev, generator=g)
+        for _ in range(3):
+            torch._int_mm(A, B.t())
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            torch._int_mm(A, B.t())
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        out["torch_int_mm"] = 2 * n ** 3 / (min(ts) * 1e-3) / 1e12
+        out["torch_int_mm_note"] = "torch._int_mm int8 [8192,8192] x [8192,8192]^T -> int32, best of 10"
+        del A, B
+    except Exception as e:
+        out["torch_int_mm_error"] = "%s: %s" % (type(e).__name__, e)
+    ok, msg, ver = pp.ptxas_accepts_tcgen05("sm_103a", "i8")
+    out["tcgen05_kind_i8_sm_103a"] = {"accepted": ok, "ptxas": msg, "ptxas_version": ver}
+    out["tcgen05_bf16_codes"] = pk["bf16_tflops"]
+    out["tcgen05_bf16_codes_note"] = ("the bf16 tcgen05 pipe carrying the INT8 codes exactly (the route this "
+                                      "library uses): MEASURED_PEAKS.json bf16 dense burst (%s)" % pk["source"])
+    cands = {k: out[k] for k in ("mma_sync_s8", "torch_int_mm", "tcgen05_bf16_codes") if k in out}
+    out["denominator"] = max(cands, key=cands.get)
+    out["denominator_tops"] = cands[out["denominator"]]
+    out["rule"] = "the largest measured rate of any exact INT8 x INT8 -> INT32 route on this GPU"
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Per-workload table (all five configurations)
+# ---------------------------------------------------------------------------
+
+def measure_workload(w8, name, dev, stream, flush, pk):
+    c = wl.CASES[name]
+    M, K, N = c.M, c.K, c.N
+    X, W, b = wl.make(c)
+    Xd, bd = X.to(dev), b.to(dev)
+    Wq, sw = w8.quantize_weight(W.to(dev))
+    Wp = w8.pack_weight(Wq)
+    ws = torch.empty(w8.workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    T = Timer(stream, flush)
+
+    def step():
+        w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=torch.cuda.current_stream())
+
+    cold = T.cold(step, PER_WORKLOAD_COLD)
+    hot = T.hot(step)
+    qg = T.cold_split([lambda: w8.linear_quant_stage(Xd, ws, stream=stream),
+                       lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)], PER_WORKLOAD_COLD)
+    st, bits_ = w8.read_status(ws)
+    if st != 0:
+        raise RuntimeError("%s: device status %d bits %#x" % (name, st, bits_))
+    Xb = Xd.to(torch.bfloat16)
+    Wb = W.to(torch.bfloat16).to(dev)
+    bb = bd.to(torch.bfloat16)
+    wsb = torch.empty(w8.bf16_linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    bf = T.cold(lambda: w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb, stream=stream), PER_WORKLOAD_COLD)
+    bf_hot = T.hot(lambda: w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb,
+                                          stream=torch.cuda.current_stream()))
+    T.release()
+    ops = c.ops
+    in_size = X.element_size()
+    bias_size = b.element_size()
+    s_cold, s_hot, q_ms, g_ms, b_ms, b_hot = med(cold), med(hot), med(qg[0]), med(qg[1]), med(bf), med(bf_hot)
+    qb = quant_bytes(M, K, in_size)
+    gb = gemm_bytes(M, N, K, bias_size)
+    # Roofline floors: the quantiser's bytes at the copy bandwidth; the GEMM at
+    # the larger of its operations at the tensor peak and its bytes at the
+    # copy bandwidth; the step = the two in sequence.
+    q_floor = qb / (pk["hbm_gbs"] * 1e9) * 1e3
+    g_floor_t = ops / (pk["bf16_tflops"] * 1e12) * 1e3
+    g_floor_m = gb / (pk["hbm_gbs"] * 1e9) * 1e3
+    g_floor = max(g_floor_t, g_floor_m)
+    plan = w8.gemm_plan(M, N, K)
+    row = {
+        "M": M, "K": K, "N": N, "x_dtype": "bf16" if in_size == 2 else "fp32", "ops": ops,
+        "step_us_cold": s_cold * 1e3, "step_us_hot": s_hot * 1e3,
+        "tops_cold": ops / (s_cold * 1e-3) / 1e12, "tops_hot": ops / (s_hot * 1e-3) / 1e12,
+        "quant_us": q_ms * 1e3, "gemm_us": g_ms * 1e3,
+        "gemm_tflops": ops / (g_ms * 1e-3) / 1e12,
+        "gemm_frac_of_tensor_peak": ops / (g_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+        "gemm_bound": "tensor" if g_floor_t >= g_floor_m else "hbm",
+        "gemm_floor_us": g_floor * 1e3, "gemm_frac_of_roofline": g_floor / g_ms,
+        "quant_gbs": qb / (q_ms * 1e-3) / 1e9, "quant_frac": qb / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "step_floor_us": (q_floor + g_floor) * 1e3, "step_frac_of_roofline_cold": (q_floor + g_floor) / s_cold,
+        "bf16_linear_us_cold": b_ms * 1e3, "bf16_linear_us_hot": b_hot * 1e3,
+        "w8a8_over_bf16_cold": b_ms / s_cold, "w8a8_over_bf16_hot": b_hot / s_hot,
+        "plan": {"dp_tiles": plan[0], "splits": plan[1], "tail_units": plan[2], "ctas": plan[3],
+                 "ctas_per_tile": plan[4]},
+        "n_cold": PER_WORKLOAD_COLD, "n_hot": PER_WORKLOAD_GRAPH * PER_WORKLOAD_REPLAYS,
+    }
+    del Xd, bd, Wq, sw, Wp, ws, Y, Xb, Wb, bb, wsb
+    return row, (X, W, b)
+
+
+PER_WORKLOAD_NOTE = (
+    "median of %d cold-L2 steps (256 MiB flush before each, events around w8a8_linear) and of %d hot-L2 "
+    "steps (%d back-to-back calls per CUDA graph, %d replays); quant_us / gemm_us: the two stage calls "
+    "after one flush, an event between them; bytes: int8 codes (1 B) as the method moves them; GEMM floor "
+    "= max(ops / bf16 tensor peak, bytes / HBM copy bandwidth); bf16_linear: the guard's native BF16 "
+    "fallback on the same shape (w8a8_over_bf16 > 1: W8A8 faster)"
+    % (PER_WORKLOAD_COLD, PER_WORKLOAD_GRAPH * PER_WORKLOAD_REPLAYS, PER_WORKLOAD_GRAPH, PER_WORKLOAD_REPLAYS))
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
@@ -344,6 +702,7 @@ def run_ours(args):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
     case = wl.CASES[args.workload]
     X, W, b = wl.make(case)
     M, K, N = case.M, case.K, case.N
@@ -355,20 +714,19 @@ def run_ours(args):
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    T = Timer(stream, flush)
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        pci = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+    except Exception:
+        pci = None
+    sampler = ClockSampler(dev.index, pci)
+    sampler.__enter__()
 
     def step():
         # One call of the hot path: w8a8_linear (quantiser, then the GEMM as
         # its programmatic dependent).
         w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=stream)
-
-    def staged(evs):
-        # The same two kernels through the two stage calls, with an event
-        # between them: each kernel's own duration (no overlap between them).
-        evs[0].record(stream)
-        w8.linear_quant_stage(Xd, ws, stream=stream)
-        evs[1].record(stream)
-        w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)
-        evs[2].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -379,93 +737,38 @@ def run_ours(args):
         raise RuntimeError("device status %d bits %#x after warm-up" % (st, bits_))
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    try:
-        pr = torch.cuda.get_device_properties(dev)
-        pci = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
-    except Exception:
-        pci = None
-    sampler = ClockSampler(dev.index, pci)
     barrier(world)
     torch.cuda.synchronize()
-    with sampler:
-        t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
-        barrier(world)
-        # per-kernel durations, for the rooflines (a second timed pass)
-        for i in range(args.steps):
-            flush.zero_()
-            staged(kevs[i])
-        torch.cuda.synchronize()
+    sampler.mark("timed_steps")
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    sampler.end("timed_steps")
     barrier(world)
     launches = 2 * args.steps
     s_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    q_ms = [e[0].elapsed_time(e[1]) for e in kevs]
-    g_ms = [e[1].elapsed_time(e[2]) for e in kevs]
     step_ms = max_over_ranks(statistics.mean(s_ms), world)
-    gemm_ms = statistics.mean(g_ms)
-    quant_ms = statistics.mean(q_ms)
     st, bits_ = w8.read_status(ws)
     if st != 0:
         raise RuntimeError("device status %d bits %#x after timed steps" % (st, bits_))
 
-    # The same step replayed from a CUDA graph (flush + w8a8_linear captured
-    # once): GPU time alone, without the binding's per-call host work, which
-    # dominates the event intervals of the small audio shapes.
-    graph = {"value": None, "ms_per_step": None}
-    try:
-        g = torch.cuda.CUDAGraph()
-        gs = torch.cuda.Stream()
-        gs.wait_stream(stream)
-        with torch.cuda.stream(gs):
-            step_on = lambda: w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=gs)  # noqa: E731
-            flush.zero_()
-            step_on()
-            gs.synchronize()
-            with torch.cuda.graph(g, stream=gs):
-                flush.zero_()
-                step_on()
-        torch.cuda.synchronize()
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(min(args.steps, 500))]
-        cur = torch.cuda.current_stream()
-        for a, b_ in gev:
-            a.record(cur)
-            g.replay()
-            b_.record(cur)
-        torch.cuda.synchronize()
-        g_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in gev)
-        # the captured step includes the 256 MiB flush: time it alone the same way
-        fg = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(gs):
-            with torch.cuda.graph(fg, stream=gs):
-                flush.zero_()
-        torch.cuda.synchronize()
-        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
-        for a, b_ in fev:
-            a.record(cur)
-            fg.replay()
-            b_.record(cur)
-        torch.cuda.synchronize()
-        f_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in fev)
-        graph = {"value": case.ops / ((g_ms - f_ms) * 1e-3) / 1e12, "ms_per_step": g_ms - f_ms,
-                 "note": "graph replay of flush + w8a8_linear, minus the flush replayed alone"}
-        st, bits_ = w8.read_status(ws)
-        if st != 0:
-            raise RuntimeError("device status %d bits %#x after graph replays" % (st, bits_))
-    except RuntimeError:
-        raise
-    except Exception as exc:  # capture unsupported: report why
-        graph = {"value": None, "ms_per_step": None, "error": "%s: %s" % (type(exc).__name__, exc)}
+    # Per-kernel durations for the rooflines: the same two kernels through
+    # the two stage calls, an event between them (no overlap between them).
+    n_split = max(args.steps, PER_WORKLOAD_COLD)
+    q_all, g_all = T.cold_split([lambda: w8.linear_quant_stage(Xd, ws, stream=stream),
+                                 lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)], n_split)
+    quant_ms, gemm_ms = med(q_all), med(g_all)
+    # Hot L2 and CUDA-graph replay of the headline step.
+    hot_ms = med(T.hot(lambda: w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=torch.cuda.current_stream())))
+    T.release()
+    st, bits_ = w8.read_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d bits %#x after the per-kernel passes" % (st, bits_))
 
     # The guard's fallback on the same shape: the native BF16 linear (the
     # same tcgen05 GEMM in its BF16 mode), each call timed alone after a flush.
@@ -475,29 +778,18 @@ def run_ours(args):
         Wb = W.to(torch.bfloat16).to(dev)
         bb = bd.to(torch.bfloat16)
         wsb = torch.empty(w8.bf16_linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            flush.zero_()
-            w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb, stream=stream)
-        bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(min(args.steps, 200))]
-        for a, b_ in bev:
-            flush.zero_()
-            a.record(stream)
-            w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb, stream=stream)
-            b_.record(stream)
-        torch.cuda.synchronize()
+        b_ms = med(T.cold(lambda: w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb, stream=stream),
+                          max(PER_WORKLOAD_COLD, min(args.steps, 200))))
         st, bits_ = w8.read_status(wsb)
         if st != 0:
             raise RuntimeError("device status %d bits %#x after BF16 linear calls" % (st, bits_))
-        b_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in bev)
         b_tf = case.ops / (b_ms * 1e-3) / 1e12
         bf16 = {"kernel": "gemm_w8a8_tcgen05_kernel (BF16 mode) via w8a8_bf16_linear", "ms": b_ms,
-                "achieved": b_tf, "unit": "TFLOP/s", "frac": b_tf / peaks()["bf16_tflops"],
-                "w8a8_step_speedup": b_ms / step_ms,
-                "note": "the guard's native BF16 fallback on this shape, header clear + GEMM, L2 flushed"}
+                "achieved": b_tf, "unit": "TFLOP/s", "frac": b_tf / pk["bf16_tflops"],
+                "w8a8_step_speedup": b_ms / med(s_ms),
+                "note": "the guard's native BF16 fallback on this shape, header clear + GEMM, L2 flushed, "
+                        "median; w8a8_step_speedup = BF16 time / W8A8 step median"}
         del Xb, Wb, bb, wsb
-
-    pk_hbm = peaks()["hbm_gbs"]
 
     # SageSLA's per-block INT8 Query/Key quantisation at the video branch's
     # attention shape (32 heads of 128 over this workload's tokens), each call
@@ -506,60 +798,56 @@ def run_ours(args):
     if M >= 1024:
         heads, dh = 32, 128
         Xqk = torch.randn((1, heads, M, dh), generator=torch.Generator().manual_seed(77)).to(torch.bfloat16).to(dev)
-        qk = {"shape": [1, heads, M, dh], "layout": "HND", "unit": "GB/s", "peak": peaks()["hbm_gbs"]}
-        for name, bt in (("query", 128), ("key", 64)):
-            for _ in range(3):
-                flush.zero_()
-                w8.quantize_qk_blocks(Xqk, bt, stream=stream)
-            qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(min(args.steps, 200))]
-            for a, b_ in qev:
-                flush.zero_()
-                a.record(stream)
-                w8.quantize_qk_blocks(Xqk, bt, stream=stream)
-                b_.record(stream)
-            torch.cuda.synchronize()
-            q_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in qev)
+        qk = {"shape": [1, heads, M, dh], "layout": "HND", "unit": "GB/s", "peak": pk["hbm_gbs"]}
+        for qname, bt in (("query", 128), ("key", 64)):
+            q_ms = med(T.cold(lambda: w8.quantize_qk_blocks(Xqk, bt, stream=stream), PER_WORKLOAD_COLD))
             nbytes = Xqk.numel() * 3 + heads * (-(-M // bt)) * 4   # bf16 in, int8 out, one scale per block
             gbs = nbytes / (q_ms * 1e-3) / 1e9
-            qk[name] = {"block_tokens": bt, "ms": q_ms, "achieved": gbs, "frac": gbs / qk["peak"],
-                        "algorithmic_bytes": nbytes}
+            qk[qname] = {"block_tokens": bt, "ms": q_ms, "achieved": gbs, "frac": gbs / qk["peak"],
+                         "algorithmic_bytes": nbytes}
         del Xqk
 
     # The norm + modulation prologue fused into the activation quantisation
     # (RMS norm, bf16 scale and shift) on this workload: the kernel alone
-    # (int8 codes) and the whole layer against the plain linear step.
+    # (int8 codes), the fused layer, and the unfused pair it replaces (a
+    # PyTorch RMS norm + modulation writing the bf16 activation, then
+    # w8a8_linear reading it).
     normp = None
     if X.dtype == torch.bfloat16:
         gn = torch.Generator().manual_seed(21)
         scn = (torch.randn(K, generator=gn) * 0.1).to(torch.bfloat16).to(dev)
         shn = (torch.randn(K, generator=gn) * 0.1).to(torch.bfloat16).to(dev)
+        ymod = torch.empty_like(Xd)
+        one_plus = (1.0 + scn.float())
+        shf = shn.float()
 
-        def timed(fn, n):
-            for _ in range(3):
-                flush.zero_()
-                fn()
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-            for a, b_ in ev:
-                flush.zero_()
-                a.record(stream)
-                fn()
-                b_.record(stream)
-            torch.cuda.synchronize()
-            return statistics.mean(a.elapsed_time(b_) for a, b_ in ev)
+        def unfused():
+            ymod.copy_(torch.nn.functional.rms_norm(Xd.float(), (K,), eps=1e-6).mul_(one_plus).add_(shf))
+            w8.linear(ymod, Wp, sw, bd, out=Y, workspace=ws, stream=stream)
 
-        n_it = min(args.steps, 200)
-        k_ms = timed(lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn, stream=stream), n_it)
-        nl_ms = timed(lambda: w8.norm_linear(Xd, Wp, sw, bd, "rms", 1e-6, scn, shn, out=Y, workspace=ws,
-                                             stream=stream), n_it)
+        def unfused_min():
+            # the least the unfused form could cost here: one bf16 write and
+            # one read of the activation on top of the plain step
+            ymod.copy_(Xd)
+            w8.linear(ymod, Wp, sw, bd, out=Y, workspace=ws, stream=stream)
+
+        k_ms = med(T.cold(lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn, stream=stream), PER_WORKLOAD_COLD))
+        nl_ms = med(T.cold(lambda: w8.norm_linear(Xd, Wp, sw, bd, "rms", 1e-6, scn, shn, out=Y, workspace=ws,
+                                                  stream=stream), PER_WORKLOAD_COLD))
+        un_ms = med(T.cold(unfused, PER_WORKLOAD_COLD))
+        um_ms = med(T.cold(unfused_min, PER_WORKLOAD_COLD))
         nbytes = M * K * 2 + M * K + M * 4 + 2 * K * 2
         normp = {"kernel": "norm_quant_rows_kernel (RMS norm, bf16 modulation, int8 codes)", "ms": k_ms,
-                 "achieved": nbytes / (k_ms * 1e-3) / 1e9, "unit": "GB/s", "peak": pk_hbm,
-                 "frac": nbytes / (k_ms * 1e-3) / 1e9 / pk_hbm, "algorithmic_bytes": nbytes,
+                 "achieved": nbytes / (k_ms * 1e-3) / 1e9, "unit": "GB/s", "peak": pk["hbm_gbs"],
+                 "frac": nbytes / (k_ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
                  "norm_linear_ms": nl_ms, "norm_linear_tops": case.ops / (nl_ms * 1e-3) / 1e12,
-                 "linear_step_ms": step_ms,
-                 "note": "w8a8_norm_linear = the prologue + GEMM in one call; the unfused form would add a "
-                         "write and a read of the modulated activation (2 B each per element)"}
+                 "unfused_torch_norm_then_linear_ms": un_ms,
+                 "unfused_copy_then_linear_ms": um_ms,
+                 "linear_step_ms": med(s_ms),
+                 "note": "medians, L2 flushed; unfused_torch: PyTorch rms_norm x (1 + scale) + shift written as bf16, "
+                         "then w8a8_linear; unfused_copy: a bf16 copy of X then w8a8_linear (a floor for any "
+                         "separate norm kernel)"}
+        del ymod
 
     # The MLP pair at the MLP workload's sizes (6144 x 4096 -> 16384 -> 4096):
     # w8a8_mlp (the down layer's codes from the up GEMM's gathered row maxima)
@@ -593,25 +881,19 @@ def run_ours(args):
 
         mlp = {"shape": {"M": Mm, "K": Km, "F": Fm, "N": Nm}, "unit": "TOPS"}
         ops_m = 2 * Mm * Fm * Km + 2 * Mm * Nm * Fm
-        for name, fn in (("fused", fused), ("separate", separate)):
-            for _ in range(3):
-                flush.zero_()
-                fn()
-            mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(min(args.steps, 50))]
-            for a, b_ in mev:
-                flush.zero_()
-                a.record(stream)
-                fn()
-                b_.record(stream)
-            torch.cuda.synchronize()
-            m_ms = statistics.mean(a.elapsed_time(b_) for a, b_ in mev)
-            mlp[name] = {"ms": m_ms, "value": ops_m / (m_ms * 1e-3) / 1e12}
+        # Interleaved, so that both see the same clock and power state.
+        f_all, s_all = [], []
+        for _ in range(5):
+            f_all += T.cold(fused, 10, warm=1)
+            s_all += T.cold(separate, 10, warm=1)
+        for mname, xs in (("fused", f_all), ("separate", s_all)):
+            mlp[mname] = {"ms": med(xs), "value": ops_m / (med(xs) * 1e-3) / 1e12, "n": len(xs)}
+        mlp["fused_speedup"] = mlp["separate"]["ms"] / mlp["fused"]["ms"]
         st, bits_ = w8.read_status(wsm)
         if st != 0:
             raise RuntimeError("device status %d bits %#x after MLP-pair calls" % (st, bits_))
         mlp["note"] = ("both layers INT8 (4 launches fused: quant, up GEMM gathering row maxima, codes pass, "
-                       "down GEMM); L2 flushed before each call")
+                       "down GEMM); L2 flushed before each call; medians of 50, the two forms interleaved")
         del Xm, Hm, Ym, wsm, wsu, wsd, Wpu, Wpd
 
     # End to end through the public C call with host buffers
@@ -659,20 +941,48 @@ def run_ours(args):
         e1.synchronize()
         floor_ms.append(e0.elapsed_time(e1))
     copy_floor = statistics.mean(floor_ms)
-    del Yd_src
+    del Yd_src, Xe
+
+    # The measured rates of the exact INT8 routes (the metric's denominator).
+    i8 = int8_peaks(dev, pk)
+
+    # Every workload of the five configurations.
+    per_wl = None
+    cpu_inputs = {}
+    if not args.no_per_workload and world == 1:
+        del ws, Y
+        torch.cuda.empty_cache()
+        per_wl = {"note": PER_WORKLOAD_NOTE}
+        for name in ["tiny", "video", "mlp_up", "mlp_down", "hires_n4k", "hires_n16k", "audio_m126_n2048",
+                     "audio_m126_n8192", "audio_m1001_n2048", "audio_m1001_n8192"]:
+            per_wl[name], host = measure_workload(w8, name, dev, stream, flush, pk)
+            if name in ("tiny", "hires_n4k", "audio_m126_n2048", "audio_m126_n8192", "audio_m1001_n2048",
+                        "audio_m1001_n8192"):
+                cpu_inputs[name] = host
+            torch.cuda.empty_cache()
+    sampler.__exit__(None, None, None)
 
     ops = case.ops
-    pk = peaks()
     gemm_tflops = ops / (gemm_ms * 1e-3) / 1e12
-    quant_bytes = M * K * X.element_size() + M * K * 2 + M * 4
-    gemm_bytes = 2 * M * K + 2 * N * K + 4 * M + 4 * N + 2 * N + 2 * M * N
-    quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
+    qb_alg = quant_bytes(M, K, X.element_size(), 1)
+    qb_built = quant_bytes(M, K, X.element_size(), 2)
+    gb_alg = gemm_bytes(M, N, K, b.element_size(), 1)
+    gb_built = gemm_bytes(M, N, K, b.element_size(), 2)
+    quant_gbs = qb_alg / (quant_ms * 1e-3) / 1e9
     clocks = sampler.summary()
+    value = world * ops / (step_ms * 1e-3) / 1e12
     if rank == 0:
-        base = cpu_baseline(case, X, W, b) if (world == 1 and not args.no_cpu_baseline) else None
+        base = None
+        base_wl = None
+        if world == 1 and not args.no_cpu_baseline:
+            base = cpu_baseline(case, X, W, b)
+            base_wl = {}
+            for name, (Xc, Wc, bc) in cpu_inputs.items():
+                c = wl.CASES[name]
+                base_wl[name] = cpu_baseline(c, Xc, Wc, bc, target_s=0.5 if name != "hires_n4k" else 4.0)
         line = {
             "metric": METRIC,
-            "value": world * ops / (step_ms * 1e-3) / 1e12,
+            "value": value,
             "unit": UNIT,
             "n_gpus": world,
             "steps": args.steps,
@@ -684,15 +994,24 @@ def run_ours(args):
             "dtype": "int8 codes x int8 codes -> int32 (exact, on bf16 tcgen05 tensor cores)",
             "data": "synthetic",
             "config": config_dict(case),
+            "step_stats_ms": {"mean": statistics.mean(s_ms), "median": med(s_ms), "min": min(s_ms),
+                              "max": max(s_ms), "n": len(s_ms), "hot_l2_graph_median": hot_ms},
+            "frac_of_int8_peak": value / world / i8["denominator_tops"],
+            "int8_peak": i8,
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
                          "traffic": GEMM_TRAFFIC.get(sources_digest(GEMM_SOURCES)) if case.name == WORKLOAD else None,
                          "kernel": "gemm_w8a8_tcgen05_kernel (GEMM + fused epilogue)",
-                         "algorithmic_bytes": gemm_bytes, "ms": gemm_ms,
+                         "algorithmic_bytes": gb_alg, "bytes_as_built": gb_built, "ms": gemm_ms,
+                         "n": len(g_all),
                          "peak_source": "%s bf16 dense burst (the MMA runs bf16 kind::f16)" % pk["source"]},
             "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                               "frac": quant_gbs / pk["hbm_gbs"], "ms": quant_ms,
-                               "kernel": "quant_rows_kernel (bf16 codes)", "algorithmic_bytes": quant_bytes},
+                               "frac": quant_gbs / pk["hbm_gbs"], "ms": quant_ms, "n": len(q_all),
+                               "kernel": "quant_rows_kernel (bf16 codes)", "algorithmic_bytes": qb_alg,
+                               "bytes_as_built": qb_built,
+                               "frac_as_built": qb_built / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                               "note": "algorithmic bytes count int8 codes (input + 1 B per code + 4 B per row); "
+                                       "the kernel writes the codes as bf16 (2 B), the tensor-core operand"},
             "e2e": {"value": world * ops / (e2e_step * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
                     "d2h_bytes_per_step": Yh.numel() * Yh.element_size(), "ms_per_step": e2e_step,
@@ -700,19 +1019,20 @@ def run_ours(args):
                     "note": "w8a8_linear_host, default chunks: copies in, compute and copies out of different "
                             "chunks overlap; copy_floor_ms = the same two transfers alone, concurrently"},
             "gpu_launches": launches,
-            "graph": graph,
             "kernel_split_ms": {"quant": quant_ms, "gemm": gemm_ms,
-                                "note": "each kernel alone (event between them); the step overlaps the "
+                                "note": "medians; each kernel alone (event between them); the step overlaps the "
                                         "GEMM's set-up with the quantiser's tail"},
             "bf16_fallback": bf16,
             "qk_block_quant": qk,
             "mlp_pair": mlp,
             "norm_prologue": normp,
+            "per_workload": per_wl,
             "clocks": clocks,
             "wall_s_timed": t_wall,
         }
         if base is not None:
             line["cpu_baseline"] = base
+            line["cpu_baseline_per_workload"] = base_wl
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -722,11 +1042,12 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(wl.CASES))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
     if args.impl == "reference":

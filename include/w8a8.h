@@ -172,6 +172,27 @@ W8A8_API size_t w8a8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 W8A8_API int w8a8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t max_slots, int64_t* plan);
 
 /* ---------------------------------------------------------------------------
+ * Which GEMM kernel the INT8 linear, the INT32 test export and the BF16
+ * linear launch for (M, N, K) (the MLP pair's up layer always takes the
+ * persistent form).  Host only; uses the current device's SM count and
+ * cluster occupancy (a 148-SM device when none is current).
+ *   form[0]  0: the persistent form whose tile schedule w8a8_gemm_plan gives;
+ *            1: the cluster-K form, for problems with few output tiles:
+ *            each 128-row x form[1]-column output tile is computed by a
+ *            thread-block cluster of form[2] CTAs that split K and add their
+ *            exact INT32 partial sums through distributed shared memory
+ *   form[1]  tile width of the cluster-K form (64, 128 or 256), else 0
+ *   form[2]  CTAs per cluster (1, 2, 4 or 8), else 0
+ *   form[3]  CTAs launched by the cluster-K form, else 0
+ * The form is chosen by estimated kernel time: the cluster-K form only for
+ * problems that leave the persistent form's single wave of 256 x 256 tiles
+ * mostly idle (the audio branch's 126- and 1001-row shapes).  Both forms
+ * compute the same exact INT32 sums and the same epilogue (identical
+ * bytes).  Returns 1, or 0 for invalid sizes.  form: int64_t[4].
+ * ------------------------------------------------------------------------- */
+W8A8_API int w8a8_gemm_form(int64_t M, int64_t N, int64_t K, int64_t* form);
+
+/* ---------------------------------------------------------------------------
  * The guarded W8A8 linear: Y = dequant(quant(X) * Wq^T) + bias, in two
  * kernels on `stream`: (1) per-row activation quantisation into the
  * workspace, (2) the tcgen05 GEMM with the fused epilogue.
@@ -237,20 +258,35 @@ W8A8_API w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t
  *    (M * K above about 33.5 million), return W8A8_ERR_WORKSPACE with
  *    nothing launched.  What the array has beyond that minimum holds the
  *    GEMM's split partial tiles.
+ *  - The array is defined in a translation unit of its own, so a process
+ *    that never calls the two entry points here does not load it (the
+ *    CUDA runtime loads modules lazily by default).
  *  - The first call on a device looks up the array's device address
- *    (once per device, with that device current).  Make that first call
- *    before any stream capture.
+ *    (once per device, with that device current) and keeps it with the
+ *    device's context; after cudaDeviceReset the next call looks it up
+ *    again.  Make that first call before any stream capture.
  *  - All calls on a device share the one array, and it keeps the previous
  *    call's contents; what must start at zero is cleared by each call.
  *    Calls that can overlap on the GPU (different streams, or threads that
  *    do not order their launches) race on the array: serialise them.
- *  - The device status word lives in the built-in array, so
- *    w8a8_read_status cannot be used with this entry point.
+ *  - The device status word lives in the built-in array: read it with
+ *    w8a8_noalloc_read_status, not w8a8_read_status.
  * ------------------------------------------------------------------------- */
 #define W8A8_NOALLOC_SCRATCH_BYTES (64ull << 20)
 W8A8_API w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K,
                                          const uint16_t* Wp, const float* sw, int64_t N,
                                          const void* bias, int bias_dtype, uint16_t* Y, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The device status word of w8a8_linear_noalloc's built-in workspace, as
+ * w8a8_read_status gives it for a caller-owned one (no paper counterpart
+ * either): waits for `stream` (synchronises it), copies the word to the host
+ * into *device_bits (W8A8_DEV_* bits), and returns W8A8_OK when it is 0,
+ * W8A8_ERR_TIMEOUT when a device-side wait of the last w8a8_linear_noalloc
+ * call on this device ran out.  Like that entry point it allocates nothing;
+ * its first call on a device looks up the array's address.
+ * ------------------------------------------------------------------------- */
+W8A8_API w8a8_status w8a8_noalloc_read_status(void* stream, uint32_t* device_bits);
 
 /* ---------------------------------------------------------------------------
  * w8a8_linear from and to HOST memory, pipelined over row chunks.
@@ -418,6 +454,13 @@ W8A8_API void w8a8_debug_skip_loads(int on);
  * single-CTA form for every M, so that tests can compare both forms on the
  * same inputs.  Results are identical either way. */
 W8A8_API void w8a8_debug_force_single_cta(int on);
+
+/* Test switch: which GEMM form every later launch takes.  form -1: chosen
+ * per shape (the default); 0: always the persistent form; 1: always the
+ * cluster-K form, with tile width bn (64, 128, 256; 0 = chosen) and cluster
+ * size ks (1, 2, 4, 8; 0 = chosen).  Used by the tests to compare the forms
+ * on the same shapes; not thread-safe with concurrent launches. */
+W8A8_API void w8a8_debug_force_gemm_form(int form, int bn, int ks);
 
 /* Static text for a status value. */
 W8A8_API const char* w8a8_status_str(int status);

@@ -32,7 +32,8 @@ def test_header_declares_the_api():
                      "w8a8_pack_weight", "w8a8_gemm_s32", "w8a8_linear_workspace_bytes",
                      "w8a8_linear_workspace_min_bytes", "w8a8_gemm_plan", "w8a8_bf16_linear",
                      "w8a8_bf16_linear_supported", "w8a8_mlp", "w8a8_norm_linear", "w8a8_norm_quantize_act",
-                     "w8a8_quantize_qk_blocks", "w8a8_linear_host", "w8a8_linear_noalloc"):
+                     "w8a8_quantize_qk_blocks", "w8a8_linear_host", "w8a8_linear_noalloc",
+                     "w8a8_noalloc_read_status"):
         assert required in names
 
 
@@ -55,6 +56,23 @@ def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(w8.lib_path())
     for name in declared_symbols():
         assert hasattr(raw, name), name
+
+
+def test_peaks_library_exports_every_declared_symbol():
+    """The throughput probes' library (roofline denominators) loads on a
+    machine without a GPU and exports what its header declares."""
+    from w8a8_int8_linear_act_b300 import build, peaks
+    build.build()
+    src = open(os.path.join(ROOT, "include", "w8a8_peaks.h")).read()
+    names = sorted(set(re.findall(r"W8A8_PEAKS_API\s+[\w\s\*]+?\b(w8a8_\w+)\s*\(", src)))
+    assert names == ["w8a8_peak_mma_sync", "w8a8_peak_mma_sync_ops"]
+    raw = ctypes.CDLL(peaks.lib_path())
+    for name in names:
+        assert hasattr(raw, name), name
+    # ops = blocks x warps x steps x 8 MMAs x (2 * 16 * 8 * 32) for INT8, (2 * 16 * 8 * 16) for bf16
+    assert peaks.mma_sync_ops(peaks.MMA_S8, 148, 256, 1000) == 148 * 8 * 1000 * 8 * 8192
+    assert peaks.mma_sync_ops(peaks.MMA_BF16, 2, 64, 3) == 2 * 2 * 3 * 8 * 4096
+    assert peaks.mma_sync_ops(peaks.MMA_S8, 1, 48, 1) == 0      # not a whole number of warps
 
 
 def test_version_and_status_strings(lib):

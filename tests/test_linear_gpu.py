@@ -14,7 +14,7 @@ import torch
 import oracle
 import w8a8_int8_linear_act_b300 as w8
 import w8a8_workloads as wl
-from helpers import assert_within_one_bf16_ulp, bias_f32, bits
+from helpers import assert_within_one_bf16_ulp, bias_f32, bits, check_linear_in_row_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -67,16 +67,31 @@ def test_linear_full_size(cuda_device, name):
 
 
 @pytest.mark.parametrize("name", ["mlp_up", "mlp_down", "hires_n4k", "hires_n16k"])
-def test_linear_full_size_sampled_rows(cuda_device, name):
-    """Full-size workloads in the launch configuration the benchmark times;
-    outputs checked on a row sample: the first and last 128-row tiles (the
-    last one ragged where M is not a multiple of 128) and 256 random rows."""
+def test_linear_full_size_every_output(cuda_device, name):
+    """The MLP and high-resolution workloads at full size, in the launch
+    configuration the benchmark times, every element checked: activation
+    and weight codes and scales bit-exact, the INT32 accumulators of the
+    same codes through w8a8_gemm_s32 bit-exact, every bf16 output within one
+    bf16 ulp of the oracle's fp32 epilogue value (and bit-identical to its
+    bf16 in practice)."""
     c = wl.CASES[name]
+    dev = cuda_device
     X, W, b = wl.make(c)
-    rng = np.random.default_rng(c.seed)
-    rows = np.unique(np.concatenate([np.arange(128), np.arange(c.M - 128, c.M),
-                                     rng.choice(c.M, 256, replace=False)]))
-    compare(X, W, b, cuda_device, rows=rows, what=name)
+    Xd = X.to(dev)
+    Wq, sw = w8.quantize_weight(W.to(dev))
+    Wp = w8.pack_weight(Wq)
+    Xq, sx = w8.quantize_act(Xd)
+    acc = w8.gemm_s32(Xq, Wp)
+    Y = w8.linear(Xd, Wp, sw, b.to(dev))
+    torch.cuda.synchronize()
+    wq_ref, sw_ref = oracle.quantize_rows(bits(W))
+    assert np.array_equal(Wq.cpu().numpy(), wq_ref)
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), sw_ref.view(np.uint32))
+    same, xq_ref, sx_ref = check_linear_in_row_blocks(bits(X), wq_ref, sw_ref, bias_f32(b), bits(Y),
+                                                      acc_gpu=acc.cpu().numpy(), what=name)
+    assert np.array_equal(Xq.cpu().numpy(), xq_ref)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_ref.view(np.uint32))
+    assert same == 1.0, "bit-identical fraction %.8f" % same
 
 
 def test_linear_no_bias_and_f32_bias(cuda_device):

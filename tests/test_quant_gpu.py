@@ -35,8 +35,12 @@ def test_act_and_weight_codes_reduced(cuda_device, name):
     check_rows(W, cuda_device, weight=True)
 
 
-@pytest.mark.parametrize("name", ["tiny", "video", "mlp_down", "audio_m1001_n8192", "audio_m126_n2048"])
+@pytest.mark.parametrize("name", ["tiny", "video", "mlp_up", "mlp_down", "hires_n4k", "hires_n16k",
+                                  "audio_m1001_n8192", "audio_m126_n2048"])
 def test_act_codes_full_size(cuda_device, name):
+    """Activation and weight codes and scales of every workload at full
+    size, bit-exact (the [16384, 4096] weights of mlp_up and hires_n16k, the
+    [28672, 4096] high-resolution activations)."""
     c = wl.CASES[name]
     X, W, _ = wl.make(c)
     q, s = check_rows(X, cuda_device)

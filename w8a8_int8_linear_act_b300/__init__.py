@@ -22,9 +22,10 @@ import torch
 __all__ = [
     "W8A8Error", "UnsupportedShape", "lib_path", "load", "shape_supported", "quantize_weight",
     "quantize_act", "pack_weight", "workspace_bytes", "workspace_min_bytes", "gemm_plan", "linear", "linear_quant_stage",
-    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "linear_host", "bf16_linear", "bf16_linear_supported",
+    "linear_gemm_stage", "gemm_s32", "linear_noalloc", "noalloc_read_status", "linear_host", "bf16_linear", "bf16_linear_supported",
     "bf16_linear_workspace_bytes", "quantize_qk_blocks", "mlp", "mlp_workspace_bytes", "norm_quantize_act",
     "norm_linear", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
+    "gemm_form", "debug_force_gemm_form",
     "W8A8Linear", "GuardedLinear", "F32", "BF16", "MAX_K",
 ]
 
@@ -83,6 +84,7 @@ def _load():
         "w8a8_linear_gemm_stage": ([i64, i64, p, p, i64, p, i32, p, p, sz, p], i32),
         "w8a8_gemm_s32": ([p, p, i64, i64, i64, p, p, sz, p], i32),
         "w8a8_linear_noalloc": ([p, i32, i64, i64, p, p, i64, p, i32, p, p], i32),
+        "w8a8_noalloc_read_status": ([p, ctypes.POINTER(ctypes.c_uint32)], i32),
         "w8a8_linear_host": ([p, i32, i64, i64, p, p, i64, p, i32, p, p, p, p, sz, i64, p], i32),
         "w8a8_bf16_linear_supported": ([i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int)], i32),
         "w8a8_bf16_linear_workspace_bytes": ([i64, i64, i64], sz),
@@ -96,6 +98,8 @@ def _load():
         "w8a8_set_wait_limit_ns": ([ctypes.c_uint64], None),
         "w8a8_debug_skip_loads": ([i32], None),
         "w8a8_debug_force_single_cta": ([i32], None),
+        "w8a8_gemm_form": ([i64, i64, i64, ctypes.POINTER(ctypes.c_int64)], i32),
+        "w8a8_debug_force_gemm_form": ([i32, i32, i32], None),
         "w8a8_status_str": ([i32], ctypes.c_char_p),
         "w8a8_version": ([], i32),
     }
@@ -201,6 +205,23 @@ def gemm_plan(M: int, N: int, K: int, num_sms: int = 0, max_slots: int = -1):
     if not _load().w8a8_gemm_plan(M, N, K, num_sms, max_slots, out):
         raise ValueError("invalid sizes for a plan: %d x %d x %d" % (M, N, K))
     return tuple(int(v) for v in out)
+
+
+def gemm_form(M: int, N: int, K: int):
+    """(form, tile width, cluster size, CTAs) of the GEMM kernel a launch
+    takes for (M, N, K): form 0 the persistent form (see ``gemm_plan``), 1
+    the cluster-K form for problems with few output tiles."""
+    out = (ctypes.c_int64 * 4)()
+    if not _load().w8a8_gemm_form(M, N, K, out):
+        raise ValueError("invalid sizes: %d x %d x %d" % (M, N, K))
+    return tuple(int(v) for v in out)
+
+
+def debug_force_gemm_form(form: int = -1, bn: int = 0, ks: int = 0):
+    """Test switch: -1 chooses the GEMM form per shape (default), 0 forces
+    the persistent form, 1 the cluster-K form (tile width bn, cluster size
+    ks; 0 = chosen)."""
+    _load().w8a8_debug_force_gemm_form(int(form), int(bn), int(ks))
 
 
 def _workspace(M, N, K, device, ws):
@@ -466,6 +487,18 @@ def linear_noalloc(X: torch.Tensor, Wp: torch.Tensor, sw: torch.Tensor, bias=Non
     _check(_load().w8a8_linear_noalloc(_ptr(X), _dt(X), M, K, _ptr(Wp), _ptr(sw), N, _ptr(bias), bdt,
                                        _ptr(out), _stream(stream)), "w8a8_linear_noalloc")
     return out
+
+
+def noalloc_read_status(stream=None):
+    """(status, device bits) of ``linear_noalloc``'s built-in workspace, as
+    ``read_status`` gives them for a caller-owned one: synchronises the
+    stream, then status 0 (OK) with bits 0, or 7 (TIMEOUT) with the
+    W8A8_DEV_* bits of the device-side waits that ran out."""
+    v = ctypes.c_uint32(0)
+    st = _load().w8a8_noalloc_read_status(_stream(stream), ctypes.byref(v))
+    if st not in (0, 7):
+        _check(st, "w8a8_noalloc_read_status")
+    return st, v.value
 
 
 def read_status(workspace: torch.Tensor, stream=None):

@@ -100,7 +100,7 @@ struct GemmCfg {
         1024 /* alignment slack */ + kStages * kStageBytes + kStagingBytes + kParamBytes + 256 /* barriers */;
 };
 static_assert(GemmCfg<1>::kSmemBytes <= 227 * 1024 && GemmCfg<2>::kSmemBytes <= 227 * 1024, "shared memory");
-static_assert((2 * GemmCfg<2>::kStages + 6) * 8 + 4 <= 256 && (2 * GemmCfg<1>::kStages + 6) * 8 + 4 <= 256,
+static_assert((2 * GemmCfg<2>::kStages + 7) * 8 + 8 <= 256 && (2 * GemmCfg<1>::kStages + 7) * 8 + 8 <= 256,
               "barrier area");
 static_assert(GemmCfg<1>::kStages * GemmCfg<1>::kStageBytes >= kPartialInt4 * 16 &&
                   GemmCfg<2>::kStages * GemmCfg<2>::kStageBytes >= kPartialInt4 * 16,
@@ -211,7 +211,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tempty = tfull + 2;             // [2] epilogue -> MMA (the leader's counts both CTAs)
     uint64_t* done = tempty + 2;              // MMA teardown
     uint64_t* fixbar = done + 1;              // split fix-up: partial tiles copied into the idle ring
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fixbar + 1);
+    uint64_t* peerbar = fixbar + 1;           // pair teardown: the peer's count of issued loads has arrived
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(peerbar + 1);
+    uint32_t* peer_issued = tmem_holder + 1;  // pair teardown: loads the peer's producer issued
     __shared__ int s_last_arrival;
     __shared__ int s_fix_status;   // split fix-up: 1 partial copied, 2 its copy timed out
     __shared__ int s_chunk_ready[2];
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(done, 1);
         mbar_init(fixbar, 1);
+        mbar_init(peerbar, 1);
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t it = 0;
-            uint32_t issued_mask = 0, issued_par = 0;
+            uint32_t n_issued = 0;   // loads issued, for iterations 0 .. n_issued - 1
             bool ok = true;
             Unit u;
             for (int ui = 0; ok && worker_unit(p, num_kb, worker, workers, ui, u); ++ui) {
@@ -297,19 +300,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tma_load_2d(sA + s * C::kAStageBytes, &tmap_a, &full[s], kb * kBK, a_row);
                         tma_load_2d(sB + s * C::kBStageBytes, &tmap_b, &full[s], kb * kBK, b_row);
                     }
-                    issued_mask |= 1u << s;
-                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    n_issued = it + 1;
                 }
             }
-            // Copies still in flight must land before the CTA exits.  The
-            // leader's "full" barriers count both CTAs' copies; the peer
-            // CTA stays until the closing cluster barrier, which the leader
-            // reaches only after these waits.
+            // Copies still in flight must land before the CTA exits.  Both
+            // producers walk the same sequence of (stage, phase) and issue
+            // the loads of iterations 0 .. n - 1, but after a timed-out wait
+            // the two counts can differ (by at most S: a producer issues
+            // iteration i only after the MMA consumed iteration i - S, which
+            // both CTAs had loaded).  In a pair every copy, the peer's too,
+            // completes on the leader's "full" barriers, so the peer sends
+            // its count to the leader, which then balances each phase the
+            // two did not both load:
+            //   loaded by the peer alone: armed now with the peer's bytes
+            //     (that stage's previous phase is complete: the MMA
+            //     consumed it before the peer could reuse the stage);
+            //   loaded by the leader alone: the missing peer bytes are
+            //     counted as complete;
+            // and waits for the last phase of every stage either issued.
+            // The peer stays until the closing cluster barrier, which the
+            // leader reaches only after these waits.
+            uint32_t n_all = n_issued;
+            if constexpr (kPair == 2) {
+                if (rank != 0) {
+                    st_cluster_u32(cluster_map(peer_issued, 0), n_issued);
+                    mbar_arrive_release_cluster(cluster_map(peerbar, 0));
+                } else {
+                    uint32_t n_peer = n_issued;
+                    if (mbar_wait_cluster(peerbar, 0, limit))
+                        n_peer = *reinterpret_cast<volatile uint32_t*>(peer_issued);
+                    else
+                        atomicOr(p.status, kDevTimeoutTeardown);
+                    for (uint32_t i = n_issued; i < n_peer; ++i)
+                        mbar_arrive_expect_tx(&full[i % S], C::kStageBytes);
+                    for (uint32_t i = n_peer; i < n_issued; ++i) mbar_complete_tx(&full[i % S], C::kStageBytes);
+                    n_all = n_peer > n_issued ? n_peer : n_issued;
+                }
+            }
             if (rank == 0)
-                for (int s = 0; s < S; ++s)
-                    if ((issued_mask >> s) & 1u)
-                        if (!mbar_wait(&full[s], (issued_par >> s) & 1u, limit))
-                            atomicOr(p.status, kDevTimeoutTeardown);
+                for (uint32_t i = n_all > static_cast<uint32_t>(S) ? n_all - S : 0u; i < n_all; ++i)
+                    if (!mbar_wait(&full[i % S], (i / S) & 1u, limit)) atomicOr(p.status, kDevTimeoutTeardown);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader CTA)

@@ -12,6 +12,7 @@
 
 #include "../../include/w8a8.h"
 #include "gemm_tcgen05.cuh"
+#include "gemm_kcluster.cuh"
 #include "quant_rows.cuh"
 #include "quant_blocks.cuh"
 #include "norm_quant.cuh"
@@ -25,6 +26,13 @@ constexpr int kMaxDevices = 64;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_skip_loads{0};
 std::atomic<int> g_force_single{0};
+std::atomic<int> g_force_form{0};    // -1: the planner decides; 0: persistent form; 1: cluster-K form
+std::atomic<int> g_force_bn{0};      // cluster-K form under the switch: tile width (0: planner's)
+std::atomic<int> g_force_ks{0};      // cluster-K form under the switch: cluster size (0: planner's)
+
+// Tile widths and cluster sizes of the cluster-K form (gemm_kcluster.cuh).
+constexpr int kKcWidths[3] = {64, 128, 256};
+constexpr int kKcSizes[4] = {1, 2, 4, 8};
 
 struct DeviceInfo {
     bool ready = false;
@@ -32,6 +40,8 @@ struct DeviceInfo {
     int num_sms = 0;
     bool gemm_attr_set = false;
     int pair_workers = 0;   // co-resident CTA pairs of the 2-CTA GEMM (0: form unavailable)
+    bool kc_ready = false;
+    int kc_clusters[3][4] = {};   // co-resident clusters of the cluster-K form per (width, cluster size)
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -227,6 +237,163 @@ GemmPlan choose_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_work
     return plan_gemm(M, N, K, 1, num_sms, max_slots);
 }
 
+// ---------------------------------------------------------------- cluster-K form
+//
+// For problems whose output has few tiles (a partial first wave of the
+// persistent form), gemm_kcluster.cuh computes each 128 x bn tile with a
+// cluster of ks CTAs that split K and add their INT32 partials through
+// distributed shared memory.  The choice compares estimated kernel times:
+//   persistent: waves of 256 x 256 pair tiles, each the MMA time of a tile;
+//   cluster-K:  per CTA the larger of its MMA time and its operand stream
+//               (128 + bn rows x its K range, 2 B per code), plus the
+//               exchange of its partial rows, times the waves of clusters
+//               that fit at once;
+// each plus a fixed per-launch cost.  Rates are per SM: the bf16 tensor
+// rate and an operand stream rate from L2 set from measurements on B300.
+struct KcPlan {
+    int bn = 0, ks = 0;
+    int64_t tiles_m = 0, tiles = 0, ctas = 0;
+    double cost_s = 0.0;
+};
+
+constexpr double kSmMmaFlops = 1.75e15 / 148.0;   // bf16 tcgen05 operations per second per SM
+constexpr double kSmStreamBps = 1.2e11;           // operand bytes per second one SM streams from L2
+constexpr double kSmExchangeBps = 2.0e11;         // partial bytes per second one SM reads from its cluster
+constexpr double kLaunchFixedS = 2.0e-6;          // set-up, pipeline fill and drain per CTA
+constexpr int kMinKbPerCta = 4;                   // at least 256 of K per CTA of a cluster
+
+int kc_width_index(int bn) { return bn == 64 ? 0 : bn == 128 ? 1 : bn == 256 ? 2 : -1; }
+int kc_size_index(int ks) { return ks == 1 ? 0 : ks == 2 ? 1 : ks == 4 ? 2 : ks == 8 ? 3 : -1; }
+
+// Estimated time of the cluster-K form with (bn, ks); `clusters`: how many
+// such clusters are co-resident.
+double kc_cost(int64_t M, int64_t N, int64_t K, int bn, int ks, int clusters, KcPlan* out)
+{
+    const int64_t tiles_m = (M + w8a8::kBM - 1) / w8a8::kBM;
+    const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+    const int64_t num_kb = (K + w8a8::kBK - 1) / w8a8::kBK;
+    const double kr = static_cast<double>((num_kb + ks - 1) / ks) * w8a8::kBK;   // K per CTA
+    const double a_rows = static_cast<double>(M < w8a8::kBM ? M : w8a8::kBM);
+    const double t_mma = 2.0 * w8a8::kBM * bn * kr / kSmMmaFlops;
+    const double t_load = (a_rows + bn) * kr * 2.0 / kSmStreamBps;
+    const double t_x = ks > 1 ? static_cast<double>(w8a8::kBM) * bn * 4.0 / kSmExchangeBps : 0.0;
+    const int64_t waves = (tiles + clusters - 1) / (clusters > 0 ? clusters : 1);
+    const double cost = static_cast<double>(waves) * ((t_mma > t_load ? t_mma : t_load) + t_x) + kLaunchFixedS;
+    if (out) {
+        out->bn = bn;
+        out->ks = ks;
+        out->tiles_m = tiles_m;
+        out->tiles = tiles;
+        out->ctas = tiles * ks;
+        out->cost_s = cost;
+    }
+    return cost;
+}
+
+// The cluster-K plan for (M, N, K), or bn == 0 when the persistent form is
+// expected to be faster.  clusters[w][s]: co-resident clusters per (width,
+// size) index.  force_bn / force_ks (nonzero) pin the width / size; `force`
+// takes the cluster-K form whatever the estimate.
+KcPlan plan_kcluster(int64_t M, int64_t N, int64_t K, int num_sms, int pair_workers, const int (*clusters)[4],
+                     bool force, int force_bn, int force_ks)
+{
+    KcPlan best;
+    const int64_t num_kb = (K + w8a8::kBK - 1) / w8a8::kBK;
+    if (!force) {
+        // Only problems that leave the persistent form's only wave mostly idle.
+        const int64_t ptiles = ((M + 255) / 256) * ((N + w8a8::kBN - 1) / w8a8::kBN);
+        if (pair_workers < 1 || ptiles * 10 > static_cast<int64_t>(pair_workers) * 6) return best;
+    }
+    double best_cost = 1e30;
+    for (int wi = 0; wi < 3; ++wi) {
+        const int bn = kKcWidths[wi];
+        if (force_bn && bn != force_bn) continue;
+        for (int si = 0; si < 4; ++si) {
+            const int ks = kKcSizes[si];
+            if (force_ks && ks != force_ks) continue;
+            if (!force_ks && ks > 1 && num_kb < static_cast<int64_t>(ks) * kMinKbPerCta) continue;
+            const int cl = clusters[wi][si];
+            if (cl < 1) continue;
+            KcPlan cand;
+            const double c = kc_cost(M, N, K, bn, ks, cl, &cand);
+            if (!force && cand.ctas > num_sms) continue;   // one wave of CTAs at most, unless forced
+            if (c < best_cost) {
+                best_cost = c;
+                best = cand;
+            }
+        }
+    }
+    if (best.bn == 0 || force) return best;
+    // Keep the persistent form where it is estimated faster: waves of pair
+    // tiles, each 256 x 256 x K of MMA work on two SMs.
+    const int64_t ptiles = ((M + 255) / 256) * ((N + w8a8::kBN - 1) / w8a8::kBN);
+    const int64_t pwaves = (ptiles + pair_workers - 1) / pair_workers;
+    const double t_pair = static_cast<double>(pwaves) * 2.0 * 256.0 * w8a8::kBN *
+                              static_cast<double>(num_kb * w8a8::kBK) / (2.0 * kSmMmaFlops) +
+                          kLaunchFixedS;
+    if (best.cost_s >= t_pair) best = KcPlan();
+    return best;
+}
+
+// Co-resident clusters when no device is current: every SM takes one CTA.
+void default_kc_clusters(int num_sms, int (*clusters)[4])
+{
+    for (int wi = 0; wi < 3; ++wi)
+        for (int si = 0; si < 4; ++si) clusters[wi][si] = num_sms / kKcSizes[si];
+}
+
+template <int kMode, int BN>
+cudaError_t set_kc_smem()
+{
+    return cudaFuncSetAttribute(w8a8::gemm_kcluster_kernel<kMode, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(w8a8::KClusterCfg<BN>::kSmemBytes));
+}
+
+template <int BN>
+int kc_max_clusters(int ks, int num_sms)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms / ks * ks));
+    cfg.blockDim = dim3(w8a8::kGemmThreads);
+    cfg.dynamicSmemBytes = w8a8::KClusterCfg<BN>::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, w8a8::gemm_kcluster_kernel<w8a8::kModeW8A8, BN>, &cfg) != cudaSuccess)
+        n = 0;
+    cudaGetLastError();
+    return n;
+}
+
+// Shared-memory attributes of the cluster-K instantiations and their
+// cluster occupancy, once per device.
+bool ensure_kcluster_ready(DeviceInfo* dev)
+{
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (dev->kc_ready) return true;
+    using namespace w8a8;
+    if (set_kc_smem<kModeW8A8, 64>() != cudaSuccess || set_kc_smem<kModeW8A8, 128>() != cudaSuccess ||
+        set_kc_smem<kModeW8A8, 256>() != cudaSuccess || set_kc_smem<kModeS32, 64>() != cudaSuccess ||
+        set_kc_smem<kModeS32, 128>() != cudaSuccess || set_kc_smem<kModeS32, 256>() != cudaSuccess ||
+        set_kc_smem<kModeBf16, 64>() != cudaSuccess || set_kc_smem<kModeBf16, 128>() != cudaSuccess ||
+        set_kc_smem<kModeBf16, 256>() != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    for (int si = 0; si < 4; ++si) {
+        dev->kc_clusters[0][si] = kc_max_clusters<64>(kKcSizes[si], dev->num_sms);
+        dev->kc_clusters[1][si] = kc_max_clusters<128>(kKcSizes[si], dev->num_sms);
+        dev->kc_clusters[2][si] = kc_max_clusters<256>(kKcSizes[si], dev->num_sms);
+    }
+    dev->kc_ready = true;
+    return true;
+}
+
 template <int kMode, int kPair>
 cudaError_t set_gemm_smem()
 {
@@ -385,6 +552,73 @@ w8a8_status launch_codes_to_bf16(const int8_t* Qi, uint16_t* Qb, int64_t n, uint
 
 // ---------------------------------------------------------------- GEMM
 
+// The cluster-K plan the GEMM launch takes for (M, N, K) on this device
+// (bn == 0: the persistent form), honouring the test switch.
+KcPlan current_kc_plan(DeviceInfo* dev, int64_t M, int64_t N, int64_t K)
+{
+    const int ff = g_force_form.load();
+    if (ff == 0) return KcPlan();
+    if (!ensure_kcluster_ready(dev)) return KcPlan();
+    KcPlan kp = plan_kcluster(M, N, K, dev->num_sms, g_force_single.load() ? 0 : dev->pair_workers, dev->kc_clusters,
+                              ff == 1, g_force_bn.load(), g_force_ks.load());
+    if (kp.ctas > INT32_MAX) kp = KcPlan();
+    return kp;
+}
+
+template <int kMode>
+w8a8_status launch_kcluster(const KcPlan& kp, const uint16_t* A_codes, const uint16_t* Wp, int64_t M, int64_t N,
+                            int64_t K, const float* sx, const float* sw, const void* bias, int bias_mode, void* out,
+                            uint32_t* status, cudaStream_t stream)
+{
+    CUtensorMap ta, tb;
+    if (!encode_bf16_2d(&ta, A_codes, M, K, w8a8::kBM)) return W8A8_ERR_CUDA;
+    if (!encode_bf16_2d(&tb, Wp, N, K, static_cast<uint32_t>(kp.bn))) return W8A8_ERR_CUDA;
+    w8a8::KClusterParams p;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.kb_per_chunk = kMode == w8a8::kModeBf16 ? static_cast<int32_t>((K + w8a8::kBK - 1) / w8a8::kBK)
+                                              : w8a8::kMaxKbPerChunk;
+    p.tiles_m = static_cast<int32_t>(kp.tiles_m);
+    p.bias_mode = bias_mode;
+    p.sx = sx;
+    p.sw = sw;
+    p.bias = bias;
+    p.out = out;
+    p.status = status;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    p.skip_loads = g_skip_loads.load();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(kp.ks);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(kp.ctas));
+    cfg.blockDim = dim3(w8a8::kGemmThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t err;
+    if (kp.bn == 64) {
+        cfg.dynamicSmemBytes = w8a8::KClusterCfg<64>::kSmemBytes;
+        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_kcluster_kernel<kMode, 64>, ta, tb, p);
+    } else if (kp.bn == 128) {
+        cfg.dynamicSmemBytes = w8a8::KClusterCfg<128>::kSmemBytes;
+        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_kcluster_kernel<kMode, 128>, ta, tb, p);
+    } else {
+        cfg.dynamicSmemBytes = w8a8::KClusterCfg<256>::kSmemBytes;
+        err = cudaLaunchKernelEx(&cfg, w8a8::gemm_kcluster_kernel<kMode, 256>, ta, tb, p);
+    }
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    return last_launch_status();
+}
+
 template <int kMode>
 w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t* Wp, int64_t M, int64_t N,
                         int64_t K, const float* sx, const float* sw, const void* bias, int bias_mode, void* out,
@@ -392,6 +626,13 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
                         uint32_t* row_amax = nullptr)
 {
     if (!ensure_gemm_ready(dev)) return W8A8_ERR_CUDA;
+    if constexpr (kMode != w8a8::kModeW8A8RowMax) {
+        // Few output tiles: the cluster-K form spreads them over the SMs.
+        const KcPlan kp = current_kc_plan(dev, M, N, K);
+        if (kp.bn != 0)
+            return launch_kcluster<kMode>(kp, A_codes, Wp, M, N, K, sx, sw, bias, bias_mode, out,
+                                          reinterpret_cast<uint32_t*>(ws_aligned + L.status_off), stream);
+    }
     const GemmPlan g = choose_plan(M, N, K, dev->num_sms, dev->pair_workers, slots);
     CUtensorMap ta, tb, ty;
     if (!encode_bf16_2d(&ta, A_codes, M, K, w8a8::kBM)) return W8A8_ERR_CUDA;
@@ -539,14 +780,6 @@ HostPipe* host_pipe(int dev)
     hp.ready = true;
     return &hp;
 }
-
-// Scratch for w8a8_linear_noalloc: a workspace built into the library for
-// callers that cannot allocate one.  Its device address is looked up once per
-// device (cudaGetSymbolAddress with that device current) and cached here;
-// host code must never use the array's name as a device pointer.
-static __device__ __align__(256) uint8_t g_noalloc_scratch[W8A8_NOALLOC_SCRATCH_BYTES];
-void* g_noalloc_ptr[kMaxDevices] = {};
-std::mutex g_noalloc_mutex;
 
 // ---------------------------------------------------------------- norm + modulation + quant
 
@@ -728,6 +961,34 @@ int w8a8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t max_slo
 
 void w8a8_debug_force_single_cta(int on) { g_force_single.store(on ? 1 : 0); }
 
+int w8a8_gemm_form(int64_t M, int64_t N, int64_t K, int64_t* form)
+{
+    if (!form || M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
+    KcPlan kp;
+    int dno = 0;
+    DeviceInfo* d = const_cast<DeviceInfo*>(device_info(&dno));
+    if (d && ensure_gemm_ready(d)) {
+        kp = current_kc_plan(d, M, N, K);
+    } else if (g_force_form.load() != 0) {
+        int cl[3][4];
+        default_kc_clusters(148, cl);
+        kp = plan_kcluster(M, N, K, 148, g_force_single.load() ? 0 : 74, cl, g_force_form.load() == 1,
+                           g_force_bn.load(), g_force_ks.load());
+    }
+    form[0] = kp.bn != 0 ? 1 : 0;
+    form[1] = kp.bn;
+    form[2] = kp.ks;
+    form[3] = kp.ctas;
+    return 1;
+}
+
+void w8a8_debug_force_gemm_form(int form, int bn, int ks)
+{
+    g_force_form.store(form < 0 ? -1 : (form == 0 ? 0 : 1));
+    g_force_bn.store(kc_width_index(bn) >= 0 ? bn : 0);
+    g_force_ks.store(kc_size_index(ks) >= 0 ? ks : 0);
+}
+
 w8a8_status w8a8_linear_quant_stage(const void* X, int x_dtype, int64_t M, int64_t K, void* ws, size_t ws_bytes,
                                     void* stream)
 {
@@ -804,35 +1065,6 @@ w8a8_status w8a8_gemm_s32(const int8_t* Xq, const uint16_t* Wp, int64_t M, int64
     return launch_gemm<w8a8::kModeS32>(dev, codes, Wp, M, N, K, nullptr, nullptr, nullptr, 0, acc, w, L,
                                        ws_slots(L, ws_bytes),
                              s);
-}
-
-w8a8_status w8a8_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp,
-                                const float* sw, int64_t N, const void* bias, int bias_dtype, uint16_t* Y,
-                                void* stream)
-{
-    WsLayout L;
-    if (M < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
-    if (ws_layout(M, K, &L) && L.min_total > W8A8_NOALLOC_SCRATCH_BYTES) return W8A8_ERR_WORKSPACE;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
-        return W8A8_ERR_NO_DEVICE;
-    }
-    void* scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-        if (g_noalloc_ptr[dev] == nullptr) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-                cudaGetLastError();
-                return W8A8_ERR_CUDA;
-            }
-            g_noalloc_ptr[dev] = p;
-        }
-        scratch = g_noalloc_ptr[dev];
-    }
-    return w8a8_linear(X, x_dtype, M, K, Wp, sw, N, bias, bias_dtype, Y, scratch, W8A8_NOALLOC_SCRATCH_BYTES,
-                       stream);
 }
 
 w8a8_status w8a8_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t K, const uint16_t* Wp,
