@@ -616,7 +616,7 @@ def int8_peaks(dev, pk):
 # Per-workload table (all five configurations)
 # ---------------------------------------------------------------------------
 
-def measure_workload(w8, name, dev, stream, flush, pk):
+def measure_workload(w8, name, dev, stream, flush, pk, sampler=None):
     c = wl.CASES[name]
     M, K, N = c.M, c.K, c.N
     X, W, b = wl.make(c)
@@ -630,8 +630,15 @@ def measure_workload(w8, name, dev, stream, flush, pk):
     def step():
         w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=torch.cuda.current_stream())
 
+    if sampler is not None:
+        sampler.mark(name + ":cold")
     cold = T.cold(step, PER_WORKLOAD_COLD)
+    if sampler is not None:
+        sampler.end(name + ":cold")
+        sampler.mark(name + ":hot")
     hot = T.hot(step)
+    if sampler is not None:
+        sampler.end(name + ":hot")
     qg = T.cold_split([lambda: w8.linear_quant_stage(Xd, ws, stream=stream),
                        lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)], PER_WORKLOAD_COLD)
     st, bits_ = w8.read_status(ws)
@@ -641,9 +648,16 @@ def measure_workload(w8, name, dev, stream, flush, pk):
     Wb = W.to(torch.bfloat16).to(dev)
     bb = bd.to(torch.bfloat16)
     wsb = torch.empty(w8.bf16_linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    if sampler is not None:
+        sampler.mark(name + ":bf16_cold")
     bf = T.cold(lambda: w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb, stream=stream), PER_WORKLOAD_COLD)
+    if sampler is not None:
+        sampler.end(name + ":bf16_cold")
+        sampler.mark(name + ":bf16_hot")
     bf_hot = T.hot(lambda: w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb,
                                           stream=torch.cuda.current_stream()))
+    if sampler is not None:
+        sampler.end(name + ":bf16_hot")
     T.release()
     ops = c.ops
     in_size = X.element_size()
@@ -659,6 +673,7 @@ def measure_workload(w8, name, dev, stream, flush, pk):
     g_floor_m = gb / (pk["hbm_gbs"] * 1e9) * 1e3
     g_floor = max(g_floor_t, g_floor_m)
     plan = w8.gemm_plan(M, N, K)
+    form = w8.gemm_form(M, N, K)
     row = {
         "M": M, "K": K, "N": N, "x_dtype": "bf16" if in_size == 2 else "fp32", "ops": ops,
         "step_us_cold": s_cold * 1e3, "step_us_hot": s_hot * 1e3,
@@ -672,8 +687,10 @@ def measure_workload(w8, name, dev, stream, flush, pk):
         "step_floor_us": (q_floor + g_floor) * 1e3, "step_frac_of_roofline_cold": (q_floor + g_floor) / s_cold,
         "bf16_linear_us_cold": b_ms * 1e3, "bf16_linear_us_hot": b_hot * 1e3,
         "w8a8_over_bf16_cold": b_ms / s_cold, "w8a8_over_bf16_hot": b_hot / s_hot,
-        "plan": {"dp_tiles": plan[0], "splits": plan[1], "tail_units": plan[2], "ctas": plan[3],
-                 "ctas_per_tile": plan[4]},
+        "gemm_form": ({"form": "cluster-K", "tile": [128, form[1]], "cluster_k": form[2], "ctas": form[3]}
+                      if form[0] == 1 else
+                      {"form": "persistent", "dp_tiles": plan[0], "splits": plan[1], "tail_units": plan[2],
+                       "ctas": plan[3], "ctas_per_tile": plan[4]}),
         "n_cold": PER_WORKLOAD_COLD, "n_hot": PER_WORKLOAD_GRAPH * PER_WORKLOAD_REPLAYS,
     }
     del Xd, bd, Wq, sw, Wp, ws, Y, Xb, Wb, bb, wsb
@@ -682,7 +699,8 @@ def measure_workload(w8, name, dev, stream, flush, pk):
 
 PER_WORKLOAD_NOTE = (
     "median of %d cold-L2 steps (256 MiB flush before each, events around w8a8_linear) and of %d hot-L2 "
-    "steps (%d back-to-back calls per CUDA graph, %d replays); quant_us / gemm_us: the two stage calls "
+    "steps (%d back-to-back calls per CUDA graph, %d replays: sustained load, where the power cap can lower "
+    "the SM clock, see clocks_hot); quant_us / gemm_us: the two stage calls "
     "after one flush, an event between them; bytes: int8 codes (1 B) as the method moves them; GEMM floor "
     "= max(ops / bf16 tensor peak, bytes / HBM copy bandwidth); bf16_linear: the guard's native BF16 "
     "fallback on the same shape (w8a8_over_bf16 > 1: W8A8 faster)"
@@ -955,7 +973,7 @@ def run_ours(args):
         per_wl = {"note": PER_WORKLOAD_NOTE}
         for name in ["tiny", "video", "mlp_up", "mlp_down", "hires_n4k", "hires_n16k", "audio_m126_n2048",
                      "audio_m126_n8192", "audio_m1001_n2048", "audio_m1001_n8192"]:
-            per_wl[name], host = measure_workload(w8, name, dev, stream, flush, pk)
+            per_wl[name], host = measure_workload(w8, name, dev, stream, flush, pk, sampler)
             if name in ("tiny", "hires_n4k", "audio_m126_n2048", "audio_m126_n8192", "audio_m1001_n2048",
                         "audio_m1001_n8192"):
                 cpu_inputs[name] = host
@@ -970,6 +988,16 @@ def run_ours(args):
     gb_built = gemm_bytes(M, N, K, b.element_size(), 2)
     quant_gbs = qb_alg / (quant_ms * 1e-3) / 1e9
     clocks = sampler.summary()
+    if per_wl is not None:
+        for name, row in per_wl.items():
+            if name == "note":
+                continue
+            for kind in ("cold", "hot", "bf16_cold", "bf16_hot"):
+                r = clocks.pop("region_%s:%s" % (name, kind), None)
+                if r is not None:
+                    row["clocks_" + kind] = {"sm_mhz": r["sm_mhz"], "sm_mhz_min": r.get("sm_mhz_min"),
+                                             "reasons": r["reasons"], "samples": r["samples"],
+                                             "power_w_max": r.get("power_w_max")}
     value = world * ops / (step_ms * 1e-3) / 1e12
     if rank == 0:
         base = None

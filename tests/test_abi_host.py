@@ -75,6 +75,31 @@ def test_peaks_library_exports_every_declared_symbol():
     assert peaks.mma_sync_ops(peaks.MMA_S8, 1, 48, 1) == 0      # not a whole number of warps
 
 
+def test_gemm_form_choice(lib):
+    """The GEMM form per shape (host-only planner, a 148-SM device when none
+    is current): the cluster-K form for the few-tile audio and tiny shapes,
+    the persistent form for the rest; the test switch pins a form."""
+    w8.debug_force_gemm_form(-1)
+    try:
+        assert w8.gemm_form(126, 2048, 2048)[0] == 1
+        assert w8.gemm_form(126, 8192, 2048)[0] == 1
+        assert w8.gemm_form(1001, 2048, 2048)[0] == 1
+        assert w8.gemm_form(64, 128, 256)[0] == 1
+        for M, N, K in [(1001, 8192, 2048), (6144, 4096, 4096), (6144, 16384, 4096), (28672, 4096, 4096)]:
+            assert w8.gemm_form(M, N, K) == (0, 0, 0, 0)
+        for M, N, K in [(126, 2048, 2048), (1001, 2048, 2048), (300, 520, 1040), (1, 8, 16)]:
+            f, bn, ks, ctas = w8.gemm_form(M, N, K)
+            if f:
+                assert bn in (64, 128, 256) and ks in (1, 2, 4, 8)
+                assert ctas == -(-M // 128) * -(-N // bn) * ks <= 148
+        w8.debug_force_gemm_form(1, 64, 8)
+        assert w8.gemm_form(300, 520, 1040) == (1, 64, 8, 3 * 9 * 8)
+        w8.debug_force_gemm_form(0)
+        assert w8.gemm_form(126, 2048, 2048) == (0, 0, 0, 0)
+    finally:
+        w8.debug_force_gemm_form(-1)
+
+
 def test_version_and_status_strings(lib):
     assert lib.w8a8_version() == 1
     for s in range(9):

@@ -2,8 +2,8 @@
 // 126- and 1001-row activations): the same exact INT32 accumulation and
 // fused epilogue as gemm_tcgen05.cuh (zhidx TurboT2VA article, section 01
 // item 3 "量化策略": INT32 accumulation, then row scale x channel scale and
-// bias applied once after the full sum; "the audio and video branches have
-// different matrix shapes"), cut so that the work spreads over the SMs.
+// bias applied once after the full sum; the audio and video branches have
+// different matrix shapes), cut so that the work spreads over the SMs.
 //
 // The persistent form gives each SM pair a 256 x 256 tile: at 126 x 2048
 // output columns that is 8 tiles for 74 pairs, and each busy pair spends the
@@ -13,24 +13,28 @@
 // taking k-blocks [r * nkb / KS, (r + 1) * nkb / KS).  Each CTA accumulates
 // its K range exactly as the persistent form does (codes carried as bf16,
 // tcgen05 kind::f16 with fp32 chunks of at most 1024 drained exactly into
-// INT32 sums in registers), writes its INT32 partial tile into its own
-// shared memory (the idle operand ring), and after a cluster barrier CTA r
-// adds, for rows [r * 128 / KS, (r + 1) * 128 / KS), the KS partials
-// through distributed shared memory (ld.shared::cluster) and runs the
-// epilogue for them.  INT32 addition is exact and associative, so the sum
-// is the exact accumulator; the bf16 linear's fp32 partials are added in
-// rank order, so its result does not depend on timing.  No global partial
-// slots, counters or fences: the exchange is one cluster barrier.
+// INT32 sums in registers).  Rank r finishes rows [r * 128 / KS, (r + 1) *
+// 128 / KS) of the tile: once every CTA of the cluster is done with its
+// operand ring (a cluster barrier), each CTA sends its partial sums of those
+// rows into rank r's ring with posted stores to distributed shared memory
+// (st.shared::cluster); after a second cluster barrier rank r adds the KS
+// partials from its own shared memory and runs the epilogue.  INT32 addition
+// is exact and associative, so the sum is the exact accumulator; the bf16
+// linear's fp32 partials are added in rank order, so its result does not
+// depend on timing.  A cluster of one keeps its sums local and needs neither
+// barrier.  No global partial slots, counters or fences.
 //
 // Roles as in the persistent form: warp 0 TMA producer, warp 1 tensor-
 // memory owner and MMA issuer (tcgen05.mma.cta_group::1 128 x BN x 16),
 // warps 2-9 epilogue (warp w reads TMEM lanes 32 * (w % 4) .. + 31 and one
-// half of the BN columns).  After the exchange the eight epilogue warps
-// split this CTA's rows into 8-column groups: consecutive threads take
-// consecutive groups of a row, so each warp stores whole 128-byte lines of Y.
-// One tile per cluster (not persistent): clusters are independent, so any
-// number of waves is correct.  Waits are bounded as in the persistent form;
-// every path through the kernel reaches both cluster barriers.
+// half of the BN columns).  While the K loop runs, the epilogue warps stage
+// the tile's sw, bias and sx in shared memory.  After the exchange they split
+// this CTA's rows into 8-column groups: consecutive threads take consecutive
+// groups of a row, so each warp stores whole 128-byte lines of Y, and every
+// operand of the epilogue is a shared-memory load.  One tile per cluster
+// (not persistent): clusters are independent, so any number of waves is
+// correct.  Waits are bounded as in the persistent form; every path through
+// the kernel reaches both cluster barriers.
 #pragma once
 
 #include <cstdint>
@@ -56,7 +60,9 @@ struct KClusterCfg {
     static constexpr uint32_t kPartBytes = kBM * kPartStride * 4;
     static constexpr uint32_t kTmemCols = 2 * BN;                         // two fp32 accumulators
     static constexpr int kLoadsPerChunk = BN / 64;                        // 32-column TMEM loads per thread
-    static constexpr size_t kSmemBytes = 1024 /* alignment */ + kStages * kStageBytes + 256 /* barriers */;
+    static constexpr uint32_t kParamBytes = (2 * BN + kBM) * 4;           // the tile's sw, bias (fp32) and sx
+    static constexpr size_t kSmemBytes =
+        1024 /* alignment */ + kStages * kStageBytes + kParamBytes + 256 /* barriers */;
     static_assert(kStages * kStageBytes >= kPartBytes, "a partial tile fits in the operand ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert((2 * kStages + 5) * 8 + 4 <= 256, "barrier area");
@@ -91,8 +97,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * C::kAStageBytes;
-    int32_t* part = reinterpret_cast<int32_t*>(smem);      // after the K loop: this CTA's INT32 partial tile
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+    int32_t* part = reinterpret_cast<int32_t*>(smem);      // after the K loop: the partial rows this CTA finishes
+    float* s_sw = reinterpret_cast<float*>(smem + S * C::kStageBytes);   // [BN] the tile's sw
+    float* s_bias = s_sw + BN;                                           // [BN] its bias as fp32 (0: none)
+    float* s_sx = s_bias + BN;                                           // [128] its rows' sx
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_sx + kBM);
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
     uint64_t* tfull = bars + 2 * S;
@@ -100,6 +109,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* done = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
     __shared__ int s_chunk_ready[2];
+    // Epilogue threads: this CTA's sums of one row half (row 32 * (warp % 4)
+    // + lane, columns (warp - 2) / 4 * BN / 2 ...), kept for the exchange.
+    int32_t acc[BN / 2];
+#pragma unroll
+    for (int i = 0; i < BN / 2; ++i) acc[i] = 0;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -207,9 +221,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int quarter = warp & 3;
         const int half = (warp - 2) >> 2;
         const int e = warp - 2;
-        int32_t acc[BN / 2];
-#pragma unroll
-        for (int i = 0; i < BN / 2; ++i) acc[i] = 0;
+        // The tile's column and row parameters into shared memory now, so
+        // that their latency hides behind the K loop.
+        for (int i = e * 32 + lane; i < BN + kBM; i += 32 * kEpiWarps) {
+            if (i < BN) {
+                const int n = nb * BN + i;
+                if constexpr (!kOutS32 && !kFp32Sums) s_sw[i] = n < p.N ? p.sw[n] : 0.0f;
+                float bv = 0.0f;
+                if (n < p.N && p.bias_mode == 1)
+                    bv = static_cast<const float*>(p.bias)[n];
+                else if (n < p.N && p.bias_mode == 2)
+                    bv = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p.bias)[n]) << 16);
+                s_bias[i] = bv;
+            } else {
+                const int m = mb * kBM + (i - BN);
+                if constexpr (!kOutS32 && !kFp32Sums) s_sx[i - BN] = m < p.M ? p.sx[m] : 0.0f;
+            }
+        }
         uint32_t cc = 0;
         for (int kc0 = kb0; kc0 < kb1; kc0 += p.kb_per_chunk, ++cc) {
             const uint32_t b = cc & 1u;
@@ -243,47 +271,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[b]);
         }
-        // This CTA's partial sums, row quarter * 32 + lane, into the idle ring
-        // (every MMA that read it is complete: its last accumulator was drained
-        // above, or on a timeout the values do not matter).
-        epi_barrier();
-        int32_t* prow = part + (quarter * 32 + lane) * C::kPartStride + half * (BN / 2);
-#pragma unroll
-        for (int g = 0; g < BN / 8; ++g)
-            *reinterpret_cast<int4*>(prow + 4 * g) = make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
     }
 
-    // Every CTA of the cluster has written its partial tile.
+    // The exchange.  Row r of the tile is finished by rank r / (128 / ks);
+    // every CTA sends its partial sums of that row to that rank, which adds
+    // the ks partials from its own shared memory.  Partials land in the
+    // receiver's operand ring, so every CTA of the cluster must be done with
+    // its ring first (barrier A: all MMAs of the cluster are complete, their
+    // last accumulators drained), and the sums must have landed before they
+    // are read (barrier B).  The sends are posted stores to distributed
+    // shared memory; all reads are local.  A cluster of one needs neither.
+    const int rows = kBM / static_cast<int>(ks);
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync_all();
+    if (ks > 1) cluster_sync_all();                                     // A
+    if (warp >= 2) {
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int r = quarter * 32 + lane;
+        const uint32_t owner = static_cast<uint32_t>(r / rows);
+        const int lr = r - static_cast<int>(owner) * rows;
+        const uint32_t off = static_cast<uint32_t>(((static_cast<int>(rank) * rows + lr) * C::kPartStride +
+                                                    half * (BN / 2)) * 4);
+        if (owner == rank) {
+            int4* dst = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(part) + off);
+#pragma unroll
+            for (int g = 0; g < BN / 8; ++g)
+                dst[g] = make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
+        } else {
+            const uint32_t dst = cluster_map(part, owner) + off;
+#pragma unroll
+            for (int g = 0; g < BN / 8; ++g)
+                st_cluster_v4(dst + 16 * g,
+                              make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
+        }
+    }
+    __syncthreads();
+    if (ks > 1) cluster_sync_all();                                     // B
     tc_fence_after_sync();
 
     if (warp >= 2) {
         // ------------------------------------------------------------ epilogue: rows of this rank
         const int t = static_cast<int>(threadIdx.x) - 64;
-        const int rows = kBM / static_cast<int>(ks);
         const int row0 = static_cast<int>(rank) * rows;
         constexpr int kGroups = BN / 8;   // 8-column groups per row
-        uint32_t pbase[kMaxClusterK];
-#pragma unroll
-        for (int j = 0; j < kMaxClusterK; ++j) pbase[j] = j < static_cast<int>(ks) ? cluster_map(part, j) : 0u;
+        const uint8_t* pbytes = reinterpret_cast<const uint8_t*>(part);
         for (int item = t; item < rows * kGroups; item += 32 * kEpiWarps) {
-            const int r = row0 + item / kGroups;
+            const int lr = item / kGroups;
             const int cg = item % kGroups;
-            const int m = mb * kBM + r;
+            const int m = mb * kBM + row0 + lr;
             const int n = nb * BN + cg * 8;
             if (m >= p.M || n >= p.N) continue;
-            const uint32_t off = static_cast<uint32_t>((r * C::kPartStride + cg * 8) * 4);
+            int4 v0[kMaxClusterK], v1[kMaxClusterK];
+#pragma unroll
+            for (int j = 0; j < kMaxClusterK; ++j) {
+                if (j < static_cast<int>(ks)) {
+                    const int4* src = reinterpret_cast<const int4*>(
+                        pbytes + ((j * rows + lr) * C::kPartStride + cg * 8) * 4);
+                    v0[j] = src[0];
+                    v1[j] = src[1];
+                } else {
+                    v0[j] = make_int4(0, 0, 0, 0);
+                    v1[j] = make_int4(0, 0, 0, 0);
+                }
+            }
             int32_t s8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) s8[i] = 0;
 #pragma unroll
             for (int j = 0; j < kMaxClusterK; ++j) {
                 if (j >= static_cast<int>(ks)) break;
-                const int4 v0 = ld_cluster_v4(pbase[j] + off);
-                const int4 v1 = ld_cluster_v4(pbase[j] + off + 16);
-                const int32_t v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                const int32_t v[8] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w, v1[j].x, v1[j].y, v1[j].z, v1[j].w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     if constexpr (kFp32Sums)
@@ -304,27 +362,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) y[i] = __int_as_float(s8[i]);
                 } else {
-                    const float sxm = p.sx[m];
-                    const float4 w0 = *reinterpret_cast<const float4*>(p.sw + n);
-                    const float4 w1 = *reinterpret_cast<const float4*>(p.sw + n + 4);
+                    const float sxm = s_sx[row0 + lr];
+                    const float4 w0 = *reinterpret_cast<const float4*>(s_sw + cg * 8);
+                    const float4 w1 = *reinterpret_cast<const float4*>(s_sw + cg * 8 + 4);
                     const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                     for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(__fmul_rn(__int2float_rn(s8[i]), sxm), wv[i]);
                 }
-                if (p.bias_mode == 1) {
-                    const float4 b0 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + n);
-                    const float4 b1 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + n + 4);
+                if (p.bias_mode != 0) {
+                    const float4 b0 = *reinterpret_cast<const float4*>(s_bias + cg * 8);
+                    const float4 b1 = *reinterpret_cast<const float4*>(s_bias + cg * 8 + 4);
                     const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
                     for (int i = 0; i < 8; ++i) y[i] = __fadd_rn(y[i], bv[i]);
-                } else if (p.bias_mode == 2) {
-                    const uint4 bb = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + n);
-                    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        y[2 * i] = __fadd_rn(y[2 * i], __uint_as_float(bw[i] << 16));
-                        y[2 * i + 1] = __fadd_rn(y[2 * i + 1], __uint_as_float(bw[i] & 0xFFFF0000u));
-                    }
                 }
                 *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + static_cast<int64_t>(m) * p.N + n) =
                     make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
@@ -333,10 +383,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     }
 
-    // No CTA leaves while another may still read its partial tile.
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync_all();
     tc_fence_after_sync();
     if (warp == 1) tmem_dealloc<1>(tmem_base, C::kTmemCols);
 }

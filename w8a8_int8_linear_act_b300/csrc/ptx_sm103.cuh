@@ -155,23 +155,14 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-// 32-bit load from the shared memory of a CTA of this cluster.
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr)
+// 16-byte store into the shared memory of a CTA of this cluster (posted:
+// the thread does not wait for it; a cluster barrier with release/acquire
+// semantics makes it visible to the receiver).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, int4 v)
 {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
-
-// 16-byte load from the shared memory of a CTA of this cluster.
-__device__ __forceinline__ int4 ld_cluster_v4(uint32_t cluster_addr)
-{
-    int4 v;
-    asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(cluster_addr)
+    asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
                  : "memory");
-    return v;
 }
 
 // As mbar_wait's single probe, with acquire semantics at cluster scope (for
@@ -245,6 +236,18 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// 4-D tiled copy global -> shared (coordinates innermost first); completion
+// is counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 

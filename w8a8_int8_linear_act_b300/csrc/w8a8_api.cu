@@ -26,9 +26,10 @@ constexpr int kMaxDevices = 64;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_skip_loads{0};
 std::atomic<int> g_force_single{0};
-std::atomic<int> g_force_form{0};    // -1: the planner decides; 0: persistent form; 1: cluster-K form
+std::atomic<int> g_force_form{-1};   // -1: the planner decides; 0: persistent form; 1: cluster-K form
 std::atomic<int> g_force_bn{0};      // cluster-K form under the switch: tile width (0: planner's)
 std::atomic<int> g_force_ks{0};      // cluster-K form under the switch: cluster size (0: planner's)
+std::atomic<int> g_force_qk_plain{1};   // Query/Key blocks: 1 = always the one-CTA-per-block kernel
 
 // Tile widths and cluster sizes of the cluster-K form (gemm_kcluster.cuh).
 constexpr int kKcWidths[3] = {64, 128, 256};
@@ -42,6 +43,7 @@ struct DeviceInfo {
     int pair_workers = 0;   // co-resident CTA pairs of the 2-CTA GEMM (0: form unavailable)
     bool kc_ready = false;
     int kc_clusters[3][4] = {};   // co-resident clusters of the cluster-K form per (width, cluster size)
+    bool qk_ready = false;        // shared-memory attributes of the Query/Key ring kernels set
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -242,50 +244,60 @@ GemmPlan choose_plan(int64_t M, int64_t N, int64_t K, int num_sms, int pair_work
 // For problems whose output has few tiles (a partial first wave of the
 // persistent form), gemm_kcluster.cuh computes each 128 x bn tile with a
 // cluster of ks CTAs that split K and add their INT32 partials through
-// distributed shared memory.  The choice compares estimated kernel times:
-//   persistent: waves of 256 x 256 pair tiles, each the MMA time of a tile;
-//   cluster-K:  per CTA the larger of its MMA time and its operand stream
-//               (128 + bn rows x its K range, 2 B per code), plus the
-//               exchange of its partial rows, times the waves of clusters
-//               that fit at once;
-// each plus a fixed per-launch cost.  Rates are per SM: the bf16 tensor
-// rate and an operand stream rate from L2 set from measurements on B300.
+// distributed shared memory.  The choice compares estimated kernel times,
+// fitted to a sweep of every (bn, ks) on B300 at the audio and tiny shapes
+// (hot L2, CUDA-graph replays):
+//   cluster-K:  a fixed cost per launch (set-up, first copies, exchange and
+//               store latency), plus per CTA its operand stream (A rows
+//               that exist + bn rows of B, 128 B per row and k-block) at the
+//               rate one SM sustains, or its MMA time if longer, plus its
+//               share of the epilogue, plus the cluster exchange (two
+//               cluster barriers) when ks > 1, times the waves of clusters;
+//   persistent: the same fixed cost plus waves of 256 x 256 pair tiles,
+//               each the MMA time of a tile.
+// Widths of 256 and clusters of 8 measured slower than the estimate in
+// every case (the 256-wide epilogue spills, clusters of 8 wait longer at
+// their barriers), so the planner uses them only under the test switch.
 struct KcPlan {
     int bn = 0, ks = 0;
     int64_t tiles_m = 0, tiles = 0, ctas = 0;
-    double cost_s = 0.0;
+    double cost_us = 0.0;
 };
 
-constexpr double kSmMmaFlops = 1.75e15 / 148.0;   // bf16 tcgen05 operations per second per SM
-constexpr double kSmStreamBps = 1.2e11;           // operand bytes per second one SM streams from L2
-constexpr double kSmExchangeBps = 2.0e11;         // partial bytes per second one SM reads from its cluster
-constexpr double kLaunchFixedS = 2.0e-6;          // set-up, pipeline fill and drain per CTA
-constexpr int kMinKbPerCta = 4;                   // at least 256 of K per CTA of a cluster
+constexpr double kSmMmaFlopsPerUs = 1.75e9 / 148.0;    // bf16 tcgen05 operations per microsecond per SM
+constexpr double kSmStreamBytesPerUs = 110e3;          // operand bytes per microsecond one SM streams
+constexpr double kLaunchFixedUs = 4.0;                 // per launch: set-up, first copies, last stores
+constexpr double kItemUs = 0.1;                        // per 8-column epilogue item of one thread
+constexpr double kExchangeUs = 1.5;                    // the cluster exchange (ks > 1)
+constexpr double kExchange4Us = 0.5;                   // ... and more for clusters of 4
+constexpr int kMinKbPerCta = 4;                        // at least 256 of K per CTA of a cluster
 
 int kc_width_index(int bn) { return bn == 64 ? 0 : bn == 128 ? 1 : bn == 256 ? 2 : -1; }
 int kc_size_index(int ks) { return ks == 1 ? 0 : ks == 2 ? 1 : ks == 4 ? 2 : ks == 8 ? 3 : -1; }
 
-// Estimated time of the cluster-K form with (bn, ks); `clusters`: how many
-// such clusters are co-resident.
+// Estimated time (microseconds) of the cluster-K form with (bn, ks);
+// `clusters`: how many such clusters are co-resident.
 double kc_cost(int64_t M, int64_t N, int64_t K, int bn, int ks, int clusters, KcPlan* out)
 {
     const int64_t tiles_m = (M + w8a8::kBM - 1) / w8a8::kBM;
     const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
     const int64_t num_kb = (K + w8a8::kBK - 1) / w8a8::kBK;
-    const double kr = static_cast<double>((num_kb + ks - 1) / ks) * w8a8::kBK;   // K per CTA
+    const double kb = static_cast<double>((num_kb + ks - 1) / ks);   // k-blocks per CTA
     const double a_rows = static_cast<double>(M < w8a8::kBM ? M : w8a8::kBM);
-    const double t_mma = 2.0 * w8a8::kBM * bn * kr / kSmMmaFlops;
-    const double t_load = (a_rows + bn) * kr * 2.0 / kSmStreamBps;
-    const double t_x = ks > 1 ? static_cast<double>(w8a8::kBM) * bn * 4.0 / kSmExchangeBps : 0.0;
+    const double t_load = kb * (a_rows + bn) * 128.0 / kSmStreamBytesPerUs;
+    const double t_mma = kb * 2.0 * w8a8::kBM * bn * w8a8::kBK / kSmMmaFlopsPerUs;
+    const double items = static_cast<double>(w8a8::kBM / ks) * (bn / 8) / (32.0 * w8a8::kEpiWarps);
+    const double t_x = ks > 1 ? kExchangeUs + (ks >= 4 ? kExchange4Us : 0.0) : 0.0;
     const int64_t waves = (tiles + clusters - 1) / (clusters > 0 ? clusters : 1);
-    const double cost = static_cast<double>(waves) * ((t_mma > t_load ? t_mma : t_load) + t_x) + kLaunchFixedS;
+    const double cost =
+        kLaunchFixedUs + static_cast<double>(waves) * ((t_mma > t_load ? t_mma : t_load) + items * kItemUs + t_x);
     if (out) {
         out->bn = bn;
         out->ks = ks;
         out->tiles_m = tiles_m;
         out->tiles = tiles;
         out->ctas = tiles * ks;
-        out->cost_s = cost;
+        out->cost_us = cost;
     }
     return cost;
 }
@@ -299,18 +311,16 @@ KcPlan plan_kcluster(int64_t M, int64_t N, int64_t K, int num_sms, int pair_work
 {
     KcPlan best;
     const int64_t num_kb = (K + w8a8::kBK - 1) / w8a8::kBK;
-    if (!force) {
-        // Only problems that leave the persistent form's only wave mostly idle.
-        const int64_t ptiles = ((M + 255) / 256) * ((N + w8a8::kBN - 1) / w8a8::kBN);
-        if (pair_workers < 1 || ptiles * 10 > static_cast<int64_t>(pair_workers) * 6) return best;
-    }
+    const int64_t ptiles = ((M + 255) / 256) * ((N + w8a8::kBN - 1) / w8a8::kBN);
+    // Only problems that leave the persistent form's only wave mostly idle.
+    if (!force && (pair_workers < 1 || ptiles * 10 > static_cast<int64_t>(pair_workers) * 6)) return best;
     double best_cost = 1e30;
     for (int wi = 0; wi < 3; ++wi) {
         const int bn = kKcWidths[wi];
-        if (force_bn && bn != force_bn) continue;
+        if (force_bn ? bn != force_bn : (!force && bn == 256)) continue;
         for (int si = 0; si < 4; ++si) {
             const int ks = kKcSizes[si];
-            if (force_ks && ks != force_ks) continue;
+            if (force_ks ? ks != force_ks : (!force && ks == 8)) continue;
             if (!force_ks && ks > 1 && num_kb < static_cast<int64_t>(ks) * kMinKbPerCta) continue;
             const int cl = clusters[wi][si];
             if (cl < 1) continue;
@@ -326,12 +336,10 @@ KcPlan plan_kcluster(int64_t M, int64_t N, int64_t K, int num_sms, int pair_work
     if (best.bn == 0 || force) return best;
     // Keep the persistent form where it is estimated faster: waves of pair
     // tiles, each 256 x 256 x K of MMA work on two SMs.
-    const int64_t ptiles = ((M + 255) / 256) * ((N + w8a8::kBN - 1) / w8a8::kBN);
     const int64_t pwaves = (ptiles + pair_workers - 1) / pair_workers;
-    const double t_pair = static_cast<double>(pwaves) * 2.0 * 256.0 * w8a8::kBN *
-                              static_cast<double>(num_kb * w8a8::kBK) / (2.0 * kSmMmaFlops) +
-                          kLaunchFixedS;
-    if (best.cost_s >= t_pair) best = KcPlan();
+    const double t_pair = kLaunchFixedUs + static_cast<double>(pwaves) * 2.0 * 256.0 * w8a8::kBN *
+                                               static_cast<double>(num_kb * w8a8::kBK) / (2.0 * kSmMmaFlopsPerUs);
+    if (best.cost_us >= t_pair) best = KcPlan();
     return best;
 }
 
@@ -847,6 +855,85 @@ w8a8_status check_norm_args(const uint16_t* X, int64_t M, int64_t K, int norm, f
 
 constexpr int kBlockThreads = 256;   // threads per CTA of the Query/Key block quantiser, at most
 
+// 4-D tensor map of a Query/Key tensor for the ring kernel (innermost
+// first): (d, token, head, batch) for the head-major layout, (d, head,
+// token, batch) for the token-major one, so the strides grow outward; boxes
+// of D x block_tokens elements, zeros past L.
+bool encode_qk_4d(CUtensorMap* map, const void* X, int x_dtype, int64_t B, int64_t H, int64_t L, int64_t D,
+                  int layout, int64_t bt)
+{
+    if (!load_encode_fn()) return false;
+    const cuuint64_t esz = x_dtype == W8A8_BF16 ? 2u : 4u;
+    const bool hnd = layout == W8A8_LAYOUT_HND;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hnd ? L : H),
+                                static_cast<cuuint64_t>(hnd ? H : L), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * esz,
+                                   static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(hnd ? L : H) * esz,
+                                   static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(H) *
+                                       static_cast<cuuint64_t>(L) * esz};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(hnd ? bt : 1),
+                               static_cast<cuuint32_t>(hnd ? 1 : bt), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = g_encode(map, x_dtype == W8A8_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                4, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool ensure_qk_ready(DeviceInfo* dev)
+{
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (dev->qk_ready) return true;
+    const int smem = static_cast<int>(w8a8::kQkRingBytes + 1024);
+    if (cudaFuncSetAttribute(w8a8::quant_blocks_ring_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess ||
+        cudaFuncSetAttribute(w8a8::quant_blocks_ring_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    dev->qk_ready = true;
+    return true;
+}
+
+// The ring form of the Query/Key block quantiser when one TMA box covers a
+// block; returns false (nothing launched) when it does not apply.
+bool launch_blocks_ring(DeviceInfo* dev, const void* X, int x_dtype, int64_t B, int64_t H, int64_t L, int64_t D,
+                        int layout, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
+                        cudaStream_t stream, w8a8_status* st)
+{
+    const int64_t esz = x_dtype == W8A8_BF16 ? 2 : 4;
+    const int64_t box_bytes = g.block_tokens * D * esz;
+    if (g_force_qk_plain.load() || D > 256 || g.block_tokens > 256 || box_bytes > 48 * 1024 || L > INT32_MAX ||
+        H > INT32_MAX || B > INT32_MAX)
+        return false;
+    if (!ensure_qk_ready(dev)) return false;
+    CUtensorMap tm;
+    if (!encode_qk_4d(&tm, X, x_dtype, B, H, L, D, layout, g.block_tokens)) return false;
+    w8a8::BlockRing rg;
+    rg.nblocks = blocks;
+    rg.box_bytes = static_cast<uint32_t>(box_bytes);
+    rg.stage_bytes = static_cast<int32_t>(align_up(static_cast<size_t>(box_bytes), 1024));
+    int stages = static_cast<int>(w8a8::kQkRingBytes / static_cast<uint32_t>(rg.stage_bytes));
+    rg.stages = stages < 2 ? 2 : (stages > w8a8::kQkMaxStages ? w8a8::kQkMaxStages : stages);
+    rg.head_major = layout == W8A8_LAYOUT_HND ? 1 : 0;
+    rg.wait_limit_ns = g_wait_limit_ns.load();
+    const size_t smem = static_cast<size_t>(rg.stages) * rg.stage_bytes + 1024;
+    // CTAs resident per SM: shared memory (228 KB per SM) and threads (2048).
+    int per_sm = static_cast<int>((228u * 1024u) / (smem + 1024));
+    if (per_sm > 8) per_sm = 8;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap = static_cast<int64_t>(dev->num_sms) * per_sm;
+    const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
+    if (x_dtype == W8A8_BF16)
+        w8a8::quant_blocks_ring_kernel<__nv_bfloat16><<<grid, w8a8::kQkRingThreads, smem, stream>>>(tm, g, rg, Q, S);
+    else
+        w8a8::quant_blocks_ring_kernel<float><<<grid, w8a8::kQkRingThreads, smem, stream>>>(tm, g, rg, Q, S);
+    *st = last_launch_status();
+    return true;
+}
+
 template <typename TIn, int NV>
 void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
                        cudaStream_t stream)
@@ -981,6 +1068,8 @@ int w8a8_gemm_form(int64_t M, int64_t N, int64_t K, int64_t* form)
     form[3] = kp.ctas;
     return 1;
 }
+
+void w8a8_debug_force_qk_plain(int on) { g_force_qk_plain.store(on ? 1 : 0); }
 
 void w8a8_debug_force_gemm_form(int form, int bn, int ks)
 {
@@ -1226,9 +1315,11 @@ w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64
     // also when block_tokens > L (then one block per head).
     const int64_t blocks = B * H * g.nblk;
     if (blocks > INT32_MAX) return W8A8_ERR_UNSUPPORTED_SHAPE;
-    const DeviceInfo* dev = device_info(nullptr);
+    DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(nullptr));
     if (!dev) return W8A8_ERR_NO_DEVICE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    w8a8_status st = W8A8_OK;
+    if (launch_blocks_ring(dev, X, x_dtype, B, H, L, D, layout, g, blocks, Xq, scales, s, &st)) return st;
     if (x_dtype == W8A8_BF16)
         return launch_blocks_typed<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(X), g, blocks, Xq, scales, s);
     return launch_blocks_typed<float>(static_cast<const float*>(X), g, blocks, Xq, scales, s);
