@@ -9,7 +9,7 @@ as its programmatic dependent.  Inputs are resident in HBM, and L2 is flushed
 the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline] [--no-per-workload]
+                  [--workload NAME] [--no-cpu-baseline] [--no-per-workload] [--profile]
 
 The JSON line also carries:
   int8_peak     the measured rates of every exact INT8 route on this GPU
@@ -505,6 +505,41 @@ class Timer:
         torch.cuda.synchronize()
         return [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(len(fns))]
 
+    def cold_graph(self, fns, n=PER_WORKLOAD_COLD, replays=3):
+        """Device time per call of each of `fns` in turn after a flush,
+        without host launch latency: graph k holds n x (flush, fns[0], ...,
+        fns[k-1]); fns[k-1] costs (T_k - T_{k-1}) / n, each T the median of
+        `replays` replays.  Returns one time (ms) per function."""
+        cur = torch.cuda.current_stream()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(self.stream)
+        totals = []
+        for k in range(len(fns) + 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(gs):
+                for f in fns[:k]:
+                    f()
+                gs.synchronize()
+                with torch.cuda.graph(g, stream=gs):
+                    for _ in range(n):
+                        self.flush.zero_()
+                        for f in fns[:k]:
+                            f()
+            torch.cuda.synchronize()
+            self.graphs.append(g)
+            g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(replays):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(cur)
+                g.replay()
+                b.record(cur)
+                b.synchronize()
+                ts.append(a.elapsed_time(b))
+            totals.append(med(ts))
+        return [(totals[k + 1] - totals[k]) / n for k in range(len(fns))]
+
     def hot(self, fn, per_graph=PER_WORKLOAD_GRAPH, replays=PER_WORKLOAD_REPLAYS):
         g = torch.cuda.CUDAGraph()
         gs = torch.cuda.Stream()
@@ -630,17 +665,19 @@ def measure_workload(w8, name, dev, stream, flush, pk, sampler=None):
     def step():
         w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=torch.cuda.current_stream())
 
+    cur = torch.cuda.current_stream
     if sampler is not None:
         sampler.mark(name + ":cold")
-    cold = T.cold(step, PER_WORKLOAD_COLD)
+    cold = T.cold_graph([step])[0]
+    cold_ev = med(T.cold(step, PER_WORKLOAD_COLD))
     if sampler is not None:
         sampler.end(name + ":cold")
         sampler.mark(name + ":hot")
     hot = T.hot(step)
     if sampler is not None:
         sampler.end(name + ":hot")
-    qg = T.cold_split([lambda: w8.linear_quant_stage(Xd, ws, stream=stream),
-                       lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)], PER_WORKLOAD_COLD)
+    qg = T.cold_graph([lambda: w8.linear_quant_stage(Xd, ws, stream=cur()),
+                       lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=cur())])
     st, bits_ = w8.read_status(ws)
     if st != 0:
         raise RuntimeError("%s: device status %d bits %#x" % (name, st, bits_))
@@ -650,7 +687,7 @@ def measure_workload(w8, name, dev, stream, flush, pk, sampler=None):
     wsb = torch.empty(w8.bf16_linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
     if sampler is not None:
         sampler.mark(name + ":bf16_cold")
-    bf = T.cold(lambda: w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb, stream=stream), PER_WORKLOAD_COLD)
+    bf = T.cold_graph([lambda: w8.bf16_linear(Xb, Wb, bb, out=Y, workspace=wsb, stream=cur())])[0]
     if sampler is not None:
         sampler.end(name + ":bf16_cold")
         sampler.mark(name + ":bf16_hot")
@@ -662,7 +699,7 @@ def measure_workload(w8, name, dev, stream, flush, pk, sampler=None):
     ops = c.ops
     in_size = X.element_size()
     bias_size = b.element_size()
-    s_cold, s_hot, q_ms, g_ms, b_ms, b_hot = med(cold), med(hot), med(qg[0]), med(qg[1]), med(bf), med(bf_hot)
+    s_cold, s_hot, q_ms, g_ms, b_ms, b_hot = cold, med(hot), qg[0], qg[1], bf, med(bf_hot)
     qb = quant_bytes(M, K, in_size)
     gb = gemm_bytes(M, N, K, bias_size)
     # Roofline floors: the quantiser's bytes at the copy bandwidth; the GEMM at
@@ -676,7 +713,7 @@ def measure_workload(w8, name, dev, stream, flush, pk, sampler=None):
     form = w8.gemm_form(M, N, K)
     row = {
         "M": M, "K": K, "N": N, "x_dtype": "bf16" if in_size == 2 else "fp32", "ops": ops,
-        "step_us_cold": s_cold * 1e3, "step_us_hot": s_hot * 1e3,
+        "step_us_cold": s_cold * 1e3, "step_us_hot": s_hot * 1e3, "step_us_cold_events": cold_ev * 1e3,
         "tops_cold": ops / (s_cold * 1e-3) / 1e12, "tops_hot": ops / (s_hot * 1e-3) / 1e12,
         "quant_us": q_ms * 1e3, "gemm_us": g_ms * 1e3,
         "gemm_tflops": ops / (g_ms * 1e-3) / 1e12,
@@ -698,13 +735,15 @@ def measure_workload(w8, name, dev, stream, flush, pk, sampler=None):
 
 
 PER_WORKLOAD_NOTE = (
-    "median of %d cold-L2 steps (256 MiB flush before each, events around w8a8_linear) and of %d hot-L2 "
-    "steps (%d back-to-back calls per CUDA graph, %d replays: sustained load, where the power cap can lower "
-    "the SM clock, see clocks_hot); quant_us / gemm_us: the two stage calls "
-    "after one flush, an event between them; bytes: int8 codes (1 B) as the method moves them; GEMM floor "
-    "= max(ops / bf16 tensor peak, bytes / HBM copy bandwidth); bf16_linear: the guard's native BF16 "
-    "fallback on the same shape (w8a8_over_bf16 > 1: W8A8 faster)"
-    % (PER_WORKLOAD_COLD, PER_WORKLOAD_GRAPH * PER_WORKLOAD_REPLAYS, PER_WORKLOAD_GRAPH, PER_WORKLOAD_REPLAYS))
+    "cold L2: a CUDA graph of %d x (256 MiB flush, call) minus one of %d flushes, per call (median of 3 "
+    "replays; no host launch latency inside), also step_us_cold_events: the median of %d event-timed "
+    "calls after a flush (host-bound for the small shapes); hot L2: %d back-to-back calls per CUDA graph, "
+    "median of %d replays (sustained load, where the power cap can lower the SM clock, see clocks_hot); "
+    "quant_us / gemm_us: the two stage calls, each the difference of graphs with and without it; bytes: "
+    "int8 codes (1 B) as the method moves them; GEMM floor = max(ops / bf16 tensor peak, bytes / HBM copy "
+    "bandwidth); bf16_linear: the guard's native BF16 fallback on the same shape (w8a8_over_bf16 > 1: W8A8 "
+    "faster)"
+    % (PER_WORKLOAD_COLD, PER_WORKLOAD_COLD, PER_WORKLOAD_COLD, PER_WORKLOAD_GRAPH, PER_WORKLOAD_REPLAYS))
 
 
 # ---------------------------------------------------------------------------
@@ -774,6 +813,18 @@ def run_ours(args):
     st, bits_ = w8.read_status(ws)
     if st != 0:
         raise RuntimeError("device status %d bits %#x after timed steps" % (st, bits_))
+    if args.profile:
+        # A short run for a profiler: the warm-up and the timed steps only.
+        sampler.__exit__(None, None, None)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": world * case.ops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+                              "ms_per_step": step_ms, "steps": args.steps, "warmup": args.warmup,
+                              "config": config_dict(case), "gemm_form": w8.gemm_form(M, N, K),
+                              "note": "--profile: warm-up and timed steps only; not a benchmark line"}), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
 
     # Per-kernel durations for the rooflines: the same two kernels through
     # the two stage calls, an event between them (no overlap between them).
@@ -1076,6 +1127,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(wl.CASES))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="warm-up and timed steps only (a short run to capture under a profiler)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
     if args.impl == "reference":

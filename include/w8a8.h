@@ -462,13 +462,6 @@ W8A8_API void w8a8_debug_force_single_cta(int on);
  * on the same shapes; not thread-safe with concurrent launches. */
 W8A8_API void w8a8_debug_force_gemm_form(int form, int bn, int ks);
 
-/* Switch between the two kernels of w8a8_quantize_qk_blocks: `on` nonzero
- * (the default) takes the one-CTA-per-block kernel for every shape; zero
- * takes the persistent kernel fed by a ring of TMA copies wherever one copy
- * covers a block (D <= 256, block_tokens <= 256, at most 48 KB).  Results
- * are identical either way; the tests compare the two. */
-W8A8_API void w8a8_debug_force_qk_plain(int on);
-
 /* Static text for a status value. */
 W8A8_API const char* w8a8_status_str(int status);
 

@@ -58,28 +58,3 @@ def test_qk_blocks_empty_and_errors(cuda_device):
     assert q.numel() == 0 and s.shape == (1, 2, 0)
     with pytest.raises(w8.UnsupportedShape):
         w8.quantize_qk_blocks(torch.zeros((1, 2, 8, 12), dtype=torch.bfloat16, device=cuda_device), 4)
-
-
-@pytest.mark.parametrize("shape,bt,layout,dtype", [
-    ((1, 32, 6144, 128), 128, "HND", torch.bfloat16),   # the bench's Query
-    ((1, 6144, 32, 128), 64, "NHD", torch.bfloat16),    # Key, token-major
-    ((2, 1001, 4, 64), 64, "NHD", torch.bfloat16),      # ragged last block
-    ((3, 5, 77, 256), 96, "HND", torch.bfloat16),       # D = 256, a 48 KB block, ragged
-    ((1, 4, 200, 64), 64, "HND", torch.float32),
-    ((2, 130, 3, 32), 7, "NHD", torch.float32),
-])
-def test_ring_and_plain_kernels_identical(cuda_device, shape, bt, layout, dtype):
-    """The persistent kernel fed by a ring of TMA copies and the
-    one-CTA-per-block kernel give the same codes and scales (and the
-    oracle's)."""
-    X = make(shape, seed=len(shape) + bt, dtype=dtype, outlier_tokens=2)
-    Xd = X.to(cuda_device)
-    w8.debug_force_qk_plain(False)
-    try:
-        q1, s1 = w8.quantize_qk_blocks(Xd, bt, layout)
-    finally:
-        w8.debug_force_qk_plain(True)
-    q2, s2 = w8.quantize_qk_blocks(Xd, bt, layout)
-    torch.cuda.synchronize()
-    assert torch.equal(q1, q2) and torch.equal(s1.view(torch.int32), s2.view(torch.int32))
-    check(X, bt, layout, cuda_device)

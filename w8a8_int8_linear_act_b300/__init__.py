@@ -25,7 +25,7 @@ __all__ = [
     "linear_gemm_stage", "gemm_s32", "linear_noalloc", "noalloc_read_status", "linear_host", "bf16_linear", "bf16_linear_supported",
     "bf16_linear_workspace_bytes", "quantize_qk_blocks", "mlp", "mlp_workspace_bytes", "norm_quantize_act",
     "norm_linear", "read_status", "set_wait_limit_ns", "debug_skip_loads", "debug_force_single_cta",
-    "gemm_form", "debug_force_gemm_form", "debug_force_qk_plain",
+    "gemm_form", "debug_force_gemm_form",
     "W8A8Linear", "GuardedLinear", "F32", "BF16", "MAX_K",
 ]
 
@@ -100,7 +100,6 @@ def _load():
         "w8a8_debug_force_single_cta": ([i32], None),
         "w8a8_gemm_form": ([i64, i64, i64, ctypes.POINTER(ctypes.c_int64)], i32),
         "w8a8_debug_force_gemm_form": ([i32, i32, i32], None),
-        "w8a8_debug_force_qk_plain": ([i32], None),
         "w8a8_status_str": ([i32], ctypes.c_char_p),
         "w8a8_version": ([], i32),
     }
@@ -223,13 +222,6 @@ def debug_force_gemm_form(form: int = -1, bn: int = 0, ks: int = 0):
     the persistent form, 1 the cluster-K form (tile width bn, cluster size
     ks; 0 = chosen)."""
     _load().w8a8_debug_force_gemm_form(int(form), int(bn), int(ks))
-
-
-def debug_force_qk_plain(on: bool):
-    """Query/Key block quantiser kernel: True (the default) always the
-    one-CTA-per-block kernel, False the persistent TMA-ring kernel where it
-    applies (results are identical)."""
-    _load().w8a8_debug_force_qk_plain(1 if on else 0)
 
 
 def _workspace(M, N, K, device, ws):

@@ -389,4 +389,5 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 1) tmem_dealloc<1>(tmem_base, C::kTmemCols);
 }
 
+
 }  // namespace w8a8

@@ -29,7 +29,6 @@ std::atomic<int> g_force_single{0};
 std::atomic<int> g_force_form{-1};   // -1: the planner decides; 0: persistent form; 1: cluster-K form
 std::atomic<int> g_force_bn{0};      // cluster-K form under the switch: tile width (0: planner's)
 std::atomic<int> g_force_ks{0};      // cluster-K form under the switch: cluster size (0: planner's)
-std::atomic<int> g_force_qk_plain{1};   // Query/Key blocks: 1 = always the one-CTA-per-block kernel
 
 // Tile widths and cluster sizes of the cluster-K form (gemm_kcluster.cuh).
 constexpr int kKcWidths[3] = {64, 128, 256};
@@ -43,7 +42,6 @@ struct DeviceInfo {
     int pair_workers = 0;   // co-resident CTA pairs of the 2-CTA GEMM (0: form unavailable)
     bool kc_ready = false;
     int kc_clusters[3][4] = {};   // co-resident clusters of the cluster-K form per (width, cluster size)
-    bool qk_ready = false;        // shared-memory attributes of the Query/Key ring kernels set
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -855,85 +853,6 @@ w8a8_status check_norm_args(const uint16_t* X, int64_t M, int64_t K, int norm, f
 
 constexpr int kBlockThreads = 256;   // threads per CTA of the Query/Key block quantiser, at most
 
-// 4-D tensor map of a Query/Key tensor for the ring kernel (innermost
-// first): (d, token, head, batch) for the head-major layout, (d, head,
-// token, batch) for the token-major one, so the strides grow outward; boxes
-// of D x block_tokens elements, zeros past L.
-bool encode_qk_4d(CUtensorMap* map, const void* X, int x_dtype, int64_t B, int64_t H, int64_t L, int64_t D,
-                  int layout, int64_t bt)
-{
-    if (!load_encode_fn()) return false;
-    const cuuint64_t esz = x_dtype == W8A8_BF16 ? 2u : 4u;
-    const bool hnd = layout == W8A8_LAYOUT_HND;
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hnd ? L : H),
-                                static_cast<cuuint64_t>(hnd ? H : L), static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * esz,
-                                   static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(hnd ? L : H) * esz,
-                                   static_cast<cuuint64_t>(D) * static_cast<cuuint64_t>(H) *
-                                       static_cast<cuuint64_t>(L) * esz};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(hnd ? bt : 1),
-                               static_cast<cuuint32_t>(hnd ? 1 : bt), 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult r = g_encode(map, x_dtype == W8A8_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                                4, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-bool ensure_qk_ready(DeviceInfo* dev)
-{
-    std::lock_guard<std::mutex> lock(g_dev_mutex);
-    if (dev->qk_ready) return true;
-    const int smem = static_cast<int>(w8a8::kQkRingBytes + 1024);
-    if (cudaFuncSetAttribute(w8a8::quant_blocks_ring_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess ||
-        cudaFuncSetAttribute(w8a8::quant_blocks_ring_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    dev->qk_ready = true;
-    return true;
-}
-
-// The ring form of the Query/Key block quantiser when one TMA box covers a
-// block; returns false (nothing launched) when it does not apply.
-bool launch_blocks_ring(DeviceInfo* dev, const void* X, int x_dtype, int64_t B, int64_t H, int64_t L, int64_t D,
-                        int layout, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
-                        cudaStream_t stream, w8a8_status* st)
-{
-    const int64_t esz = x_dtype == W8A8_BF16 ? 2 : 4;
-    const int64_t box_bytes = g.block_tokens * D * esz;
-    if (g_force_qk_plain.load() || D > 256 || g.block_tokens > 256 || box_bytes > 48 * 1024 || L > INT32_MAX ||
-        H > INT32_MAX || B > INT32_MAX)
-        return false;
-    if (!ensure_qk_ready(dev)) return false;
-    CUtensorMap tm;
-    if (!encode_qk_4d(&tm, X, x_dtype, B, H, L, D, layout, g.block_tokens)) return false;
-    w8a8::BlockRing rg;
-    rg.nblocks = blocks;
-    rg.box_bytes = static_cast<uint32_t>(box_bytes);
-    rg.stage_bytes = static_cast<int32_t>(align_up(static_cast<size_t>(box_bytes), 1024));
-    int stages = static_cast<int>(w8a8::kQkRingBytes / static_cast<uint32_t>(rg.stage_bytes));
-    rg.stages = stages < 2 ? 2 : (stages > w8a8::kQkMaxStages ? w8a8::kQkMaxStages : stages);
-    rg.head_major = layout == W8A8_LAYOUT_HND ? 1 : 0;
-    rg.wait_limit_ns = g_wait_limit_ns.load();
-    const size_t smem = static_cast<size_t>(rg.stages) * rg.stage_bytes + 1024;
-    // CTAs resident per SM: shared memory (228 KB per SM) and threads (2048).
-    int per_sm = static_cast<int>((228u * 1024u) / (smem + 1024));
-    if (per_sm > 8) per_sm = 8;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t cap = static_cast<int64_t>(dev->num_sms) * per_sm;
-    const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-    if (x_dtype == W8A8_BF16)
-        w8a8::quant_blocks_ring_kernel<__nv_bfloat16><<<grid, w8a8::kQkRingThreads, smem, stream>>>(tm, g, rg, Q, S);
-    else
-        w8a8::quant_blocks_ring_kernel<float><<<grid, w8a8::kQkRingThreads, smem, stream>>>(tm, g, rg, Q, S);
-    *st = last_launch_status();
-    return true;
-}
-
 template <typename TIn, int NV>
 void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
                        cudaStream_t stream)
@@ -1068,8 +987,6 @@ int w8a8_gemm_form(int64_t M, int64_t N, int64_t K, int64_t* form)
     form[3] = kp.ctas;
     return 1;
 }
-
-void w8a8_debug_force_qk_plain(int on) { g_force_qk_plain.store(on ? 1 : 0); }
 
 void w8a8_debug_force_gemm_form(int form, int bn, int ks)
 {
@@ -1315,11 +1232,9 @@ w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64
     // also when block_tokens > L (then one block per head).
     const int64_t blocks = B * H * g.nblk;
     if (blocks > INT32_MAX) return W8A8_ERR_UNSUPPORTED_SHAPE;
-    DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(nullptr));
+    const DeviceInfo* dev = device_info(nullptr);
     if (!dev) return W8A8_ERR_NO_DEVICE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    w8a8_status st = W8A8_OK;
-    if (launch_blocks_ring(dev, X, x_dtype, B, H, L, D, layout, g, blocks, Xq, scales, s, &st)) return st;
     if (x_dtype == W8A8_BF16)
         return launch_blocks_typed<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(X), g, blocks, Xq, scales, s);
     return launch_blocks_typed<float>(static_cast<const float*>(X), g, blocks, Xq, scales, s);
