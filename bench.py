@@ -77,7 +77,7 @@ def gemm_bytes(M, N, K, bias_size=2, code_size=1):
 # code has changed since.
 GEMM_SOURCES = ["w8a8_int8_linear_act_b300/csrc/gemm_tcgen05.cuh",
                 "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh"]
-GEMM_TRAFFIC = {"4c6119a28db36d2a": 164.14e6}
+GEMM_TRAFFIC = {"4c6119a28db36d2a": 164.14e6, "fd3b36ebdcdd6b15": 167.30e6}
 
 
 def sources_digest(paths):
@@ -505,15 +505,17 @@ class Timer:
         torch.cuda.synchronize()
         return [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(len(fns))]
 
-    def cold_graph(self, fns, n=PER_WORKLOAD_COLD, replays=3):
+    def cold_graph(self, fns, n=PER_WORKLOAD_COLD, replays=7):
         """Device time per call of each of `fns` in turn after a flush,
         without host launch latency: graph k holds n x (flush, fns[0], ...,
         fns[k-1]); fns[k-1] costs (T_k - T_{k-1}) / n, each T the median of
-        `replays` replays.  Returns one time (ms) per function."""
+        `replays` replays, the graphs replayed in turn (so that slow drifts
+        of the clock fall on all of them alike).  Returns one time (ms) per
+        function."""
         cur = torch.cuda.current_stream()
         gs = torch.cuda.Stream()
         gs.wait_stream(self.stream)
-        totals = []
+        graphs = []
         for k in range(len(fns) + 1):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(gs):
@@ -527,17 +529,19 @@ class Timer:
                             f()
             torch.cuda.synchronize()
             self.graphs.append(g)
+            graphs.append(g)
             g.replay()
-            torch.cuda.synchronize()
-            ts = []
-            for _ in range(replays):
+        torch.cuda.synchronize()
+        ts = [[] for _ in graphs]
+        for _ in range(replays):
+            for k, g in enumerate(graphs):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(cur)
                 g.replay()
                 b.record(cur)
                 b.synchronize()
-                ts.append(a.elapsed_time(b))
-            totals.append(med(ts))
+                ts[k].append(a.elapsed_time(b))
+        totals = [med(t) for t in ts]
         return [(totals[k + 1] - totals[k]) / n for k in range(len(fns))]
 
     def hot(self, fn, per_graph=PER_WORKLOAD_GRAPH, replays=PER_WORKLOAD_REPLAYS):
@@ -828,10 +832,18 @@ def run_ours(args):
 
     # Per-kernel durations for the rooflines: the same two kernels through
     # the two stage calls, an event between them (no overlap between them).
+    # Each kernel's duration: the difference of CUDA graphs of n x (flush,
+    # quantiser) and n x (flush, quantiser, GEMM) replays (no host launch
+    # latency; the GEMM keeps its programmatic overlap with the quantiser),
+    # and, beside it, event intervals around the two stage calls.
     n_split = max(args.steps, PER_WORKLOAD_COLD)
+    cur = torch.cuda.current_stream
+    quant_ms, gemm_ms = T.cold_graph([lambda: w8.linear_quant_stage(Xd, ws, stream=cur()),
+                                      lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=cur())], n_split)
+    T.release()
     q_all, g_all = T.cold_split([lambda: w8.linear_quant_stage(Xd, ws, stream=stream),
                                  lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)], n_split)
-    quant_ms, gemm_ms = med(q_all), med(g_all)
+    quant_ev_ms, gemm_ev_ms = med(q_all), med(g_all)
     # Hot L2 and CUDA-graph replay of the headline step.
     hot_ms = med(T.hot(lambda: w8.linear(Xd, Wp, sw, bd, out=Y, workspace=ws, stream=torch.cuda.current_stream())))
     T.release()
@@ -1082,10 +1094,13 @@ def run_ours(args):
                          "traffic": GEMM_TRAFFIC.get(sources_digest(GEMM_SOURCES)) if case.name == WORKLOAD else None,
                          "kernel": "gemm_w8a8_tcgen05_kernel (GEMM + fused epilogue)",
                          "algorithmic_bytes": gb_alg, "bytes_as_built": gb_built, "ms": gemm_ms,
-                         "n": len(g_all),
+                         "n": n_split, "ms_events": gemm_ev_ms,
+                         "timing": "graph replays: n x (flush, quantiser, GEMM) minus n x (flush, quantiser), "
+                                   "per launch; ms_events: median event interval around the stage call",
                          "peak_source": "%s bf16 dense burst (the MMA runs bf16 kind::f16)" % pk["source"]},
             "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                               "frac": quant_gbs / pk["hbm_gbs"], "ms": quant_ms, "n": len(q_all),
+                               "frac": quant_gbs / pk["hbm_gbs"], "ms": quant_ms, "n": n_split,
+                               "ms_events": quant_ev_ms,
                                "kernel": "quant_rows_kernel (bf16 codes)", "algorithmic_bytes": qb_alg,
                                "bytes_as_built": qb_built,
                                "frac_as_built": qb_built / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
@@ -1098,9 +1113,11 @@ def run_ours(args):
                     "note": "w8a8_linear_host, default chunks: copies in, compute and copies out of different "
                             "chunks overlap; copy_floor_ms = the same two transfers alone, concurrently"},
             "gpu_launches": launches,
-            "kernel_split_ms": {"quant": quant_ms, "gemm": gemm_ms,
-                                "note": "medians; each kernel alone (event between them); the step overlaps the "
-                                        "GEMM's set-up with the quantiser's tail"},
+            "kernel_split_ms": {"quant": quant_ms, "gemm": gemm_ms, "quant_events": quant_ev_ms,
+                                "gemm_events": gemm_ev_ms,
+                                "note": "per launch from graph replays (see roofline.timing); *_events: medians of "
+                                        "event intervals around each stage call (they include the launch after "
+                                        "the event that separates the two kernels)"},
             "bf16_fallback": bf16,
             "qk_block_quant": qk,
             "mlp_pair": mlp,

@@ -148,3 +148,30 @@ def test_bf16_linear_guarded_layer_dispatch(cuda_device):
     ref = oracle.linear(bits(X), wq, sw, bias_f32(b))
     yg = oracle.bf16_bits_to_f32(bits(Y)).astype(np.float64)
     assert (np.abs(yg - ref["y32"]) <= oracle.ulp_bf16(ref["y32"])).all()
+
+
+def test_guarded_layer_fastest_policy(cuda_device):
+    """policy="fastest": per row count, the layer times both paths once and
+    keeps the faster; each call's output is then exactly that path's output
+    (the W8A8 path within one bf16 ulp of the oracle, the BF16 path within
+    its accumulation bound)."""
+    X, W, b = make(300, 512, 1024, seed=9)
+    dev = cuda_device
+    layer = w8.GuardedLinear(W.to(dev), b.to(dev), policy="fastest")
+    assert layer.int8
+    Y = layer(X.to(dev))
+    torch.cuda.synchronize()
+    choice = layer.choice[(300, torch.bfloat16)]
+    assert choice in ("int8", "bf16")
+    if choice == "int8":
+        wq, sw = oracle.quantize_rows(bits(W))
+        ref = oracle.linear(bits(X), wq, sw, bias_f32(b))
+        yg = oracle.bf16_bits_to_f32(bits(Y)).astype(np.float64)
+        assert (np.abs(yg - ref["y32"]) <= oracle.ulp_bf16(ref["y32"])).all()
+    else:
+        check(Y.cpu(), X, W, b)
+    Y2 = layer(X.to(dev))          # the cached choice, same bytes
+    torch.cuda.synchronize()
+    assert torch.equal(Y2.view(torch.int16), Y.view(torch.int16))
+    with pytest.raises(ValueError):
+        w8.GuardedLinear(W.to(dev), b.to(dev), policy="sometimes")

@@ -551,10 +551,28 @@ class GuardedLinear:
     accumulation) where it does not: the guarded W8A8 layer of the TurboT2VA
     pages (zhidx article, section 01 item 3; arXiv paper, appendix C).
     The choice per layer follows from (N, K, bias dtype); per call, a row
-    count the guard rejects also takes the BF16 path."""
+    count the guard rejects also takes the BF16 path.
 
-    def __init__(self, weight: torch.Tensor, bias=None):
+    ``policy``:
+      "int8"     (default) the W8A8 path wherever the guard accepts: the method
+                 as the pages give it.
+      "fastest"  per row count, whichever of the two paths is faster on this
+                 GPU, timed (CUDA events, median of 5 calls each after 3
+                 warm-up calls) on the first call with that row count and
+                 kept.  On B300 the bf16 tensor pipe carries both paths, so
+                 W8A8 wins only where its lower power draw holds the clock
+                 up under the power cap (the longest GEMMs) and loses where
+                 the activation quantisation is a large share of the call.
+                 Both outputs are correct; they differ by the quantisation
+                 error.  Needs a bfloat16 weight (kept for the BF16 path)."""
+
+    POLICIES = ("int8", "fastest")
+
+    def __init__(self, weight: torch.Tensor, bias=None, policy: str = "int8"):
         _cuda2d(weight, "weight")
+        if policy not in self.POLICIES:
+            raise ValueError("policy must be one of %s" % (self.POLICIES,))
+        self.policy = policy
         self.out_features, self.in_features = weight.shape
         bdt = bias.dtype if bias is not None else torch.bfloat16
         self.int8 = shape_supported(1, self.out_features, self.in_features, torch.bfloat16, bdt)[0]
@@ -562,17 +580,43 @@ class GuardedLinear:
         self.weight = weight if weight.dtype == torch.bfloat16 else None
         self._w8a8 = W8A8Linear(weight, bias) if self.int8 else None
         self._ws = None
-        if not self.int8 and self.weight is None:
-            raise TypeError("a layer the INT8 guard rejects runs the BF16 linear: pass a bfloat16 weight")
+        self.choice = {}   # (rows, activation dtype) -> "int8" or "bf16", for policy "fastest"
+        if (not self.int8 or policy == "fastest") and self.weight is None:
+            raise TypeError("the BF16 path of this layer needs a bfloat16 weight")
+
+    def _bf16(self, X: torch.Tensor, out=None) -> torch.Tensor:
+        M = X.shape[0]
+        need = bf16_linear_workspace_bytes(M, self.out_features, self.in_features)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=X.device)
+        Xb = X if X.dtype == torch.bfloat16 else X.to(torch.bfloat16)
+        return bf16_linear(Xb, self.weight, self.bias, out=out, workspace=self._ws)
+
+    def _fastest(self, X: torch.Tensor) -> str:
+        key = (X.shape[0], X.dtype)
+        if key not in self.choice:
+            stream = torch.cuda.current_stream()
+            times = {}
+            for name, fn in (("int8", lambda: self._w8a8(X)), ("bf16", lambda: self._bf16(X))):
+                for _ in range(3):
+                    fn()
+                ts = []
+                for _ in range(5):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    b.synchronize()
+                    ts.append(a.elapsed_time(b))
+                times[name] = sorted(ts)[2]
+            self.choice[key] = "int8" if times["int8"] <= times["bf16"] else "bf16"
+        return self.choice[key]
 
     def __call__(self, X: torch.Tensor, out=None) -> torch.Tensor:
         M = X.shape[0]
         if self._w8a8 is not None and self._w8a8.supported(M, X.dtype):
-            return self._w8a8(X, out=out)
+            if self.policy == "int8" or self._fastest(X) == "int8":
+                return self._w8a8(X, out=out)
         if self.weight is None:
             raise UnsupportedShape(4, "GuardedLinear: no bfloat16 weight kept for the BF16 path")
-        need = bf16_linear_workspace_bytes(M, self.out_features, self.in_features)
-        if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=X.device)
-        return bf16_linear(X, self.weight, self.bias, out=out, workspace=self._ws)
-
+        return self._bf16(X, out=out)

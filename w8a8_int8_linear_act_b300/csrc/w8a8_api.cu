@@ -488,12 +488,33 @@ void launch_quant_cfg(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uin
 // threads per row reading it twice.
 constexpr int kQuantRows = 4;
 
+// Fewer rows than this many per SM: a CTA per row of at most 256 threads with
+// 2, 4 or 8 vectors a thread (rows of 64 to 2048 vectors), so that the few
+// rows spread over the SMs instead of filling a handful of them a warp per
+// row.
+constexpr int64_t kFewRowsPerSm = 2;
+
 template <typename TIn, bool kBf16Codes>
 w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header,
-                               cudaStream_t stream, uint32_t* zero_rows)
+                               cudaStream_t stream, uint32_t* zero_rows, int num_sms)
 {
     constexpr int E = w8a8::InVec<TIn>::kElems;
     const int64_t V = K / E;  // vectors per row
+    if (R <= kFewRowsPerSm * num_sms && V >= 64 && V <= 2048) {
+        if (V <= 512)
+            launch_quant_cfg<TIn, kBf16Codes, 2, 0>(A, R, K, Q, S, header,
+                                                    static_cast<unsigned>(((V + 1) / 2 + 31) / 32 * 32), stream,
+                                                    zero_rows);
+        else if (V <= 1024)
+            launch_quant_cfg<TIn, kBf16Codes, 4, 0>(A, R, K, Q, S, header,
+                                                    static_cast<unsigned>(((V + 3) / 4 + 31) / 32 * 32), stream,
+                                                    zero_rows);
+        else
+            launch_quant_cfg<TIn, kBf16Codes, 8, 0>(A, R, K, Q, S, header,
+                                                    static_cast<unsigned>(((V + 7) / 8 + 31) / 32 * 32), stream,
+                                                    zero_rows);
+        return last_launch_status();
+    }
     if (V <= 32)
         launch_quant_cfg<TIn, kBf16Codes, 1, kQuantRows>(A, R, K, Q, S, header, 32 * kQuantRows, stream, zero_rows);
     else if (V <= 64)
@@ -516,11 +537,13 @@ template <bool kBf16Codes>
 w8a8_status launch_quant(const void* A, int dtype, int64_t R, int64_t K, void* Q, float* S, uint32_t* status,
                          cudaStream_t stream, uint32_t* zero_rows = nullptr)
 {
+    const DeviceInfo* dev = device_info(nullptr);
+    const int num_sms = dev ? dev->num_sms : 148;
     if (dtype == W8A8_BF16)
         return launch_quant_typed<__nv_bfloat16, kBf16Codes>(static_cast<const __nv_bfloat16*>(A), R, K, Q, S,
-                                                             status, stream, zero_rows);
+                                                             status, stream, zero_rows, num_sms);
     return launch_quant_typed<float, kBf16Codes>(static_cast<const float*>(A), R, K, Q, S, status, stream,
-                                                 zero_rows);
+                                                 zero_rows, num_sms);
 }
 
 w8a8_status check_quant_args(const void* A, int dtype, int64_t R, int64_t K, const void* Q, const float* S)
