@@ -473,6 +473,8 @@ class Timer:
     def __init__(self, stream, flush):
         self.stream = stream
         self.flush = flush
+        self.flush2 = None    # the clean flush's second buffer, made on first use
+        self.sink = torch.zeros((), dtype=torch.int64, device=flush.device)
         self.graphs = []      # captured graphs stay alive with the buffers they use, until release()
 
     def cold(self, fn, n, warm=3):
@@ -505,7 +507,16 @@ class Timer:
         torch.cuda.synchronize()
         return [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(len(fns))]
 
-    def cold_graph(self, fns, n=PER_WORKLOAD_COLD, replays=7):
+    def clean_flush(self):
+        """The write flush, then a read of a second buffer of the same size,
+        so that L2 is left holding clean lines (the next kernel's misses then
+        evict without writing back)."""
+        self.flush.zero_()
+        if self.flush2 is None:
+            self.flush2 = torch.ones_like(self.flush)
+        torch.sum(self.flush2.view(torch.int32), dim=0, dtype=torch.int64, out=self.sink)
+
+    def cold_graph(self, fns, n=PER_WORKLOAD_COLD, replays=7, clean=False):
         """Device time per call of each of `fns` in turn after a flush,
         without host launch latency: graph k holds n x (flush, fns[0], ...,
         fns[k-1]); fns[k-1] costs (T_k - T_{k-1}) / n, each T the median of
@@ -524,7 +535,10 @@ class Timer:
                 gs.synchronize()
                 with torch.cuda.graph(g, stream=gs):
                     for _ in range(n):
-                        self.flush.zero_()
+                        if clean:
+                            self.clean_flush()
+                        else:
+                            self.flush.zero_()
                         for f in fns[:k]:
                             f()
             torch.cuda.synchronize()
@@ -841,6 +855,8 @@ def run_ours(args):
     quant_ms, gemm_ms = T.cold_graph([lambda: w8.linear_quant_stage(Xd, ws, stream=cur()),
                                       lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=cur())], n_split)
     T.release()
+    quant_clean_ms = T.cold_graph([lambda: w8.linear_quant_stage(Xd, ws, stream=cur())], n_split, clean=True)[0]
+    T.release()
     q_all, g_all = T.cold_split([lambda: w8.linear_quant_stage(Xd, ws, stream=stream),
                                  lambda: w8.linear_gemm_stage(M, K, Wp, sw, bd, Y, ws, stream=stream)], n_split)
     quant_ev_ms, gemm_ev_ms = med(q_all), med(g_all)
@@ -882,10 +898,14 @@ def run_ours(args):
         qk = {"shape": [1, heads, M, dh], "layout": "HND", "unit": "GB/s", "peak": pk["hbm_gbs"]}
         for qname, bt in (("query", 128), ("key", 64)):
             q_ms = med(T.cold(lambda: w8.quantize_qk_blocks(Xqk, bt, stream=stream), PER_WORKLOAD_COLD))
+            qc_ms = T.cold_graph([lambda: w8.quantize_qk_blocks(Xqk, bt, stream=torch.cuda.current_stream())],
+                                 PER_WORKLOAD_COLD, clean=True)[0]
+            T.release()
             nbytes = Xqk.numel() * 3 + heads * (-(-M // bt)) * 4   # bf16 in, int8 out, one scale per block
             gbs = nbytes / (q_ms * 1e-3) / 1e9
             qk[qname] = {"block_tokens": bt, "ms": q_ms, "achieved": gbs, "frac": gbs / qk["peak"],
-                         "algorithmic_bytes": nbytes}
+                         "algorithmic_bytes": nbytes,
+                         "clean_l2": {"ms": qc_ms, "frac": nbytes / (qc_ms * 1e-3) / 1e9 / qk["peak"]}}
         del Xqk
 
     # The norm + modulation prologue fused into the activation quantisation
@@ -913,6 +933,10 @@ def run_ours(args):
             w8.linear(ymod, Wp, sw, bd, out=Y, workspace=ws, stream=stream)
 
         k_ms = med(T.cold(lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn, stream=stream), PER_WORKLOAD_COLD))
+        kc_ms = T.cold_graph([lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn,
+                                                           stream=torch.cuda.current_stream())],
+                             PER_WORKLOAD_COLD, clean=True)[0]
+        T.release()
         nl_ms = med(T.cold(lambda: w8.norm_linear(Xd, Wp, sw, bd, "rms", 1e-6, scn, shn, out=Y, workspace=ws,
                                                   stream=stream), PER_WORKLOAD_COLD))
         un_ms = med(T.cold(unfused, PER_WORKLOAD_COLD))
@@ -921,6 +945,7 @@ def run_ours(args):
         normp = {"kernel": "norm_quant_rows_kernel (RMS norm, bf16 modulation, int8 codes)", "ms": k_ms,
                  "achieved": nbytes / (k_ms * 1e-3) / 1e9, "unit": "GB/s", "peak": pk["hbm_gbs"],
                  "frac": nbytes / (k_ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
+                 "clean_l2": {"ms": kc_ms, "frac": nbytes / (kc_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
                  "norm_linear_ms": nl_ms, "norm_linear_tops": case.ops / (nl_ms * 1e-3) / 1e12,
                  "unfused_torch_norm_then_linear_ms": un_ms,
                  "unfused_copy_then_linear_ms": um_ms,
@@ -1101,6 +1126,12 @@ def run_ours(args):
             "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                "frac": quant_gbs / pk["hbm_gbs"], "ms": quant_ms, "n": n_split,
                                "ms_events": quant_ev_ms,
+                               "clean_l2": {"ms": quant_clean_ms,
+                                            "frac": qb_alg / (quant_clean_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                            "frac_as_built": qb_built / (quant_clean_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                            "note": "after a flush that writes 256 MiB and then reads another "
+                                                    "256 MiB, so L2 holds clean lines: the kernel's misses evict "
+                                                    "without the write-backs the write flush's dirty lines cost"},
                                "kernel": "quant_rows_kernel (bf16 codes)", "algorithmic_bytes": qb_alg,
                                "bytes_as_built": qb_built,
                                "frac_as_built": qb_built / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
