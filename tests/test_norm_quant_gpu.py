@@ -106,6 +106,9 @@ def mod_vectors(K, seed, dtype):
     (5, 32768, "rms", torch.float32),       # the largest K
     (33, 1040, "rms", torch.bfloat16),      # ragged vector count per lane
     (3, 16, "layer", torch.float32),        # the smallest K: two vectors per row
+    (129, 1024, "rms", torch.bfloat16),     # whole rows of 4 vectors per lane
+    (77, 2048, "rms", torch.float32),       # whole rows of 8 vectors per lane
+    (3001, 1040, "layer", torch.bfloat16),  # more rows than warps on the GPU, ragged lanes
 ])
 def test_norm_quant_shapes(cuda_device, M, K, kind, mod):
     g = torch.Generator().manual_seed(M + K)

@@ -18,11 +18,16 @@
 // optionally also written out.  The unfused form would write y (2 B per
 // element) and read it back for the quantiser; here the row is read once.
 //
-// Structure: as the quantiser (a warp per row, four rows per CTA, up to 16
-// vectors per lane, for K <= 4096; a CTA per row up to 32768), with the row
-// held in registers through three reductions: the sum (LayerNorm), the sum
-// of squared deviations, and the absmax of y.  In the warp form the CTA
-// prepares the modulation once in shared memory as fp32 (1 + scale, shift).
+// Structure: as the quantiser (a warp per row, up to 16 vectors per lane,
+// for K <= 4096; a CTA per row up to 32768), with the row held in registers
+// through three reductions: the sum (LayerNorm), the sum of squared
+// deviations, and the absmax of y.  The warp form is persistent: CTAs of
+// eight warps, as many as fit on the GPU at once, each preparing the
+// modulation once in shared memory as fp32 (1 + scale, shift); each warp
+// works through rows grid-stride, and copies its next row into a buffer of
+// its own in shared memory while the current row's arithmetic runs, so that
+// HBM keeps streaming during the arithmetic.  The per-element arithmetic
+// runs on packed pairs of fp32 (f32x2), one instruction for two elements.
 #pragma once
 
 #include <cstdint>
@@ -113,109 +118,223 @@ __device__ __forceinline__ void keep_packed(uint4 (&v)[NV])
     for (int i = 0; i < NV; ++i) asm volatile("" : "+r"(v[i].x), "+r"(v[i].y), "+r"(v[i].z), "+r"(v[i].w));
 }
 
-template <bool kBf16Codes, int NV, int kRowsPerCta, int kNorm>
-__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRowsPerCta > 1 ? 20 / kRowsPerCta : 1)
-    norm_quant_rows_kernel(const __nv_bfloat16* __restrict__ A, int64_t R, int64_t K, NormParams np,
-                           void* __restrict__ Q, float* __restrict__ S, uint32_t* __restrict__ header)
+// Two independent fp32 operations in one instruction (sm_100 and later);
+// each half is rounded exactly as the scalar operation would round it, so
+// the packed forms change no result, only the instruction count.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Both bf16 of a 32-bit word as fp32 (low half first).
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// quantize_vector of quant_rows.cuh on one vector of y, in packed pairs:
+// t = fma(y, r, M), the residual fma(y, r, M - t) and its check, with the
+// same scalar fallback by division near a tie.
+// kWarpUniform: all 32 lanes of the warp call this together, so the rare
+// near-tie branch is taken by the whole warp or by none (one vote, no
+// divergence bookkeeping).
+template <bool kBf16Codes, bool kWarpUniform>
+__device__ __forceinline__ void quantize_vector_x2(const uint4& vec, const RowScale& rs, void* Q, int64_t off)
+{
+    const uint32_t w[4] = {vec.x, vec.y, vec.z, vec.w};
+    const float2 rr = make_float2(rs.r, rs.r), mm = make_float2(kRoundMagic, kRoundMagic);
+    float t[8], nq[8];
+    float dmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 x = bf16x2_to_f2(w[i]);
+        const float2 tt = fma2(x, rr, mm);
+        const float2 n = sub2(mm, tt);           // minus the code, exactly
+        const float2 res = fma2(x, rr, n);
+        dmax = fmaxf(dmax, fmaxf(fabsf(res.x), fabsf(res.y)));
+        t[2 * i] = tt.x;
+        t[2 * i + 1] = tt.y;
+        nq[2 * i] = n.x;
+        nq[2 * i + 1] = n.y;
+    }
+    const bool slow = dmax > kNearHalf || rs.exact;
+    if (kWarpUniform ? __any_sync(0xFFFFFFFFu, slow) : slow) {
+        float x[8];
+        InVec<__nv_bfloat16>::unpack(vec, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (rs.exact || fabsf(__fmaf_rn(x[e], rs.r, nq[e])) > kNearHalf)
+                t[e] = __fadd_rn(code_by_division(x[e], rs.s), kRoundMagic);
+    }
+    if constexpr (kBf16Codes) {
+        // q = t - M, as the scalar form computes it (+0 for a zero code).
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 qq = sub2(make_float2(t[2 * i], t[2 * i + 1]), mm);
+            q[2 * i] = qq.x;
+            q[2 * i + 1] = qq.y;
+        }
+        store_codes<true, 8>(Q, off, q);
+    } else {
+        store_codes<false, 8>(Q, off, t);
+    }
+}
+
+// Copies lane t's vectors t, t + 32, ... of row `row` into the warp's
+// buffer in shared memory (one commit group).
+template <int NV, bool kFull>
+__device__ __forceinline__ void copy_row_async(const __nv_bfloat16* __restrict__ A, int64_t row, int64_t K,
+                                               uint4* buf, int t)
+{
+    const int V = static_cast<int>(K / 8);
+    const uint4* src = reinterpret_cast<const uint4*>(A + row * K);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int idx = t + i * 32;
+        if (kFull || idx < V) cp_async_16(buf + idx, src + idx);
+    }
+    cp_async_commit();
+}
+
+// One row: thread t of T holds vectors t, t + T, ... of the row.
+// kWarp: the row belongs to one warp (T = 32).  Its vectors are already on
+// their way into the warp's shared-memory buffer `buf` (copy_row_async);
+// once the first pass has taken them into registers, the copy of `next`
+// (when not negative), the warp's following row, is started into the same
+// buffer, so that it streams in while this row's arithmetic runs.  The
+// modulation is staged in s_mod.
+// Otherwise the row belongs to the whole CTA, is loaded straight into
+// registers, reduces block-wide, and reads the modulation per vector.
+// kFull: the row is exactly NV vectors per lane of the warp (K = 256 NV),
+// so no lane has a vector out of range.
+template <bool kBf16Codes, int NV, bool kWarp, bool kFull, int kNorm>
+__device__ __forceinline__ void norm_quant_row(const __nv_bfloat16* __restrict__ A, int64_t row, int64_t next,
+                                               int64_t K, const NormParams& np, void* __restrict__ Q,
+                                               float* __restrict__ S, int t, int T, const float4* s_mod,
+                                               uint4* buf, float* red_sum, float* red_sq, float* red_max)
 {
     using IV = InVec<__nv_bfloat16>;
-    __shared__ float red_sum[32], red_sq[32], red_max[32];
-
-    grid_launch_dependents();
-    if (header != nullptr && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
-
-    const bool has_sc = np.scale != nullptr, has_sh = np.shift != nullptr;
-    // Warp form: the CTA first turns the modulation into fp32 a = 1 + scale
-    // (1 without scale) and b = shift (-0 without shift, which leaves every
-    // sum unchanged) in shared memory, as four float4 arrays of V entries
-    // (elements 0-3 and 4-7 of each vector apart, so that lanes reading
-    // neighbouring vectors hit distinct banks).  fma(x r, 1, -0) and
-    // fma(x r, a, -0) equal x r and (x r) a exactly, so y = fma(x r, a, b)
-    // takes the same roundings as the steps it stands for.
-    extern __shared__ float4 s_mod[];
-    const int Vall = static_cast<int>(K / 8);
-    if constexpr (kRowsPerCta > 1) {
-        for (int k8 = threadIdx.x; k8 < Vall; k8 += blockDim.x) {
-            float sc[8], sh[8];
-            if (has_sc) unpack_mod(load_mod(np.scale, np.mod_f32, k8), np.mod_f32, sc);
-            if (has_sh) unpack_mod(load_mod(np.shift, np.mod_f32, k8), np.mod_f32, sh);
-            float a[8], b[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                a[e] = has_sc ? __fadd_rn(1.0f, sc[e]) : 1.0f;
-                b[e] = has_sh ? sh[e] : -0.0f;
-            }
-            s_mod[k8] = make_float4(a[0], a[1], a[2], a[3]);
-            s_mod[Vall + k8] = make_float4(a[4], a[5], a[6], a[7]);
-            s_mod[2 * Vall + k8] = make_float4(b[0], b[1], b[2], b[3]);
-            s_mod[3 * Vall + k8] = make_float4(b[4], b[5], b[6], b[7]);
-        }
-        __syncthreads();
-    }
-
-    const int64_t row = kRowsPerCta > 1 ? static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5)
-                                        : static_cast<int64_t>(blockIdx.x);
-    if (kRowsPerCta > 1 && row >= R) return;   // warp-uniform; no block-wide barrier follows
-    const int T = kRowsPerCta > 1 ? 32 : static_cast<int>(blockDim.x);
-    const int t = kRowsPerCta > 1 ? static_cast<int>(threadIdx.x & 31) : static_cast<int>(threadIdx.x);
     const int V = static_cast<int>(K / 8);
     const uint4* src = reinterpret_cast<const uint4*>(A + row * K);
     const int64_t out0 = row * K;
     const float kf = static_cast<float>(K);
 
     uint4 v[NV];
+    if constexpr (kWarp) {
+        cp_async_wait_all();   // this lane's own copies: no exchange between lanes
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int idx = t + i * T;
-        v[i] = (idx < V) ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < NV; ++i) {
+            const int idx = t + i * T;
+            v[i] = (kFull || idx < V) ? buf[idx] : make_uint4(0, 0, 0, 0);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int idx = t + i * T;
+            v[i] = (kFull || idx < V) ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
+        }
     }
+    // The first pass below reads every v[i], so this lane's shared-memory
+    // reads have returned before its copies of the next row overwrite them.
+    auto start_next = [&]() {
+        if constexpr (kWarp) {
+            if (next >= 0) copy_row_async<NV, kFull>(A, next, K, buf, t);
+        }
+    };
 
     // Each sum runs in eight independent partial sums per thread (one per
     // element position of a vector), so the adds do not form one long
     // dependent chain; the partials are then added pairwise.
     float mu = 0.0f;
     if constexpr (kNorm == kNormLayer) {
-        float p8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        float2 p2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                        make_float2(0.0f, 0.0f)};
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            float x[8];
-            IV::unpack(v[i], x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) p8[e] = __fadd_rn(p8[e], x[e]);   // padding vectors are zero
+        for (int i = 0; i < NV; ++i) {   // padding vectors are zero
+            p2[0] = add2(p2[0], bf16x2_to_f2(v[i].x));
+            p2[1] = add2(p2[1], bf16x2_to_f2(v[i].y));
+            p2[2] = add2(p2[2], bf16x2_to_f2(v[i].z));
+            p2[3] = add2(p2[3], bf16x2_to_f2(v[i].w));
         }
+        const float p8[8] = {p2[0].x, p2[0].y, p2[1].x, p2[1].y, p2[2].x, p2[2].y, p2[3].x, p2[3].y};
+        start_next();
         float s = sum8(p8);
-        s = kRowsPerCta > 1 ? warp_sum(s) : block_sum(s, red_sum);
+        s = kWarp ? warp_sum(s) : block_sum(s, red_sum);
         mu = __fdiv_rn(s, kf);
         keep_packed(v);
     }
-    float q8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    float2 q2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                    make_float2(0.0f, 0.0f)};
+    const float2 mu2 = make_float2(mu, mu);
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-        if (t + i * T < V) {
-            float x[8];
-            IV::unpack(v[i], x);
+        if (kFull || t + i * T < V) {
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float d = kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e];
-                q8[e] = __fmaf_rn(d, d, q8[e]);
+            for (int j = 0; j < 4; ++j) {
+                float2 d = bf16x2_to_f2(w[j]);
+                if constexpr (kNorm == kNormLayer) d = sub2(d, mu2);
+                q2[j] = fma2(d, d, q2[j]);
             }
         }
     }
+    const float q8[8] = {q2[0].x, q2[0].y, q2[1].x, q2[1].y, q2[2].x, q2[2].y, q2[3].x, q2[3].y};
+    if constexpr (kNorm != kNormLayer) start_next();
     float q = sum8(q8);
-    q = kRowsPerCta > 1 ? warp_sum(q) : block_sum(q, red_sq);
+    q = kWarp ? warp_sum(q) : block_sum(q, red_sq);
     keep_packed(v);
     const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(q, kf), np.eps));
 
     // y, rounded to bf16, replaces x in the registers.
+    const bool has_sc = np.scale != nullptr, has_sh = np.shift != nullptr;
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int idx = t + i * T;
-        if (idx < V) {
+        if (kFull || idx < V) {
             float x[8], a[8], b[8];
             IV::unpack(v[i], x);
-            if constexpr (kRowsPerCta > 1) {
+            if constexpr (kWarp) {
                 const float4 a0 = s_mod[idx], a1 = s_mod[V + idx];
                 const float4 b0 = s_mod[2 * V + idx], b1 = s_mod[3 * V + idx];
                 a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
@@ -232,24 +351,100 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRow
                     b[e] = has_sh ? sh[e] : -0.0f;
                 }
             }
-            float y[8];
+            uint32_t yw[4];
+            const float2 r2 = make_float2(r, r);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                y[e] = __fmaf_rn(__fmul_rn(kNorm == kNormLayer ? __fsub_rn(x[e], mu) : x[e], r), a[e], b[e]);
-            v[i] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                              pack_bf16x2(y[6], y[7]));
+            for (int j = 0; j < 4; ++j) {
+                float2 d = make_float2(x[2 * j], x[2 * j + 1]);
+                if constexpr (kNorm == kNormLayer) d = sub2(d, mu2);
+                const float2 y = fma2(mul2(d, r2), make_float2(a[2 * j], a[2 * j + 1]),
+                                      make_float2(b[2 * j], b[2 * j + 1]));
+                yw[j] = pack_bf16x2(y.x, y.y);
+            }
+            v[i] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
             if (np.y_out != nullptr)
                 *reinterpret_cast<uint4*>(np.y_out + out0 + static_cast<int64_t>(idx) * 8) = v[i];
             IV::absmax(v[i], m2);
         }
     }
-    const float amax = kRowsPerCta > 1 ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red_max);
+    const float amax = kWarp ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red_max);
     const RowScale rs = row_scale(amax);
     if (t == 0) S[row] = rs.s;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int idx = t + i * T;
-        if (idx < V) quantize_vector<__nv_bfloat16, kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+        if (kFull || idx < V)
+            quantize_vector_x2<kBf16Codes, kFull>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+    }
+}
+
+// kRowsPerCta > 1 (warp form): a CTA of kRowsPerCta warps stages the
+// modulation once, then each warp takes rows warp, warp + stride, ... of the
+// whole grid (stride = gridDim.x * kRowsPerCta); the launcher sizes the
+// grid to the CTAs that fit on the GPU at once, so that every warp works
+// through several rows, its next row streaming into its shared-memory
+// buffer while it computes on the current one.  Dynamic shared memory:
+// the modulation (8 B per element of a row), then a row buffer per warp
+// (2 B per element).  kRowsPerCta == 1: a CTA per row (long rows).
+// kFull (warp form only): K = 256 NV.
+template <bool kBf16Codes, int NV, int kRowsPerCta, bool kFull, int kNorm>
+__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRowsPerCta > 1 ? 2 : 1)
+    norm_quant_rows_kernel(const __nv_bfloat16* __restrict__ A, int64_t R, int64_t K, NormParams np,
+                           void* __restrict__ Q, float* __restrict__ S, uint32_t* __restrict__ header)
+{
+    __shared__ float red_sum[32], red_sq[32], red_max[32];
+
+    grid_launch_dependents();
+    if (header != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
+
+    // Warp form: the CTA first turns the modulation into fp32 a = 1 + scale
+    // (1 without scale) and b = shift (-0 without shift, which leaves every
+    // sum unchanged) in shared memory, as four float4 arrays of V entries
+    // (elements 0-3 and 4-7 of each vector apart, so that lanes reading
+    // neighbouring vectors hit distinct banks).  fma(x r, 1, -0) and
+    // fma(x r, a, -0) equal x r and (x r) a exactly, so y = fma(x r, a, b)
+    // takes the same roundings as the steps it stands for.
+    extern __shared__ float4 s_mod[];
+    if constexpr (kRowsPerCta > 1) {
+        const bool has_sc = np.scale != nullptr, has_sh = np.shift != nullptr;
+        const int V = static_cast<int>(K / 8);
+        for (int k8 = threadIdx.x; k8 < V; k8 += blockDim.x) {
+            float a[8], b[8];
+            if (has_sc) {
+                unpack_mod(load_mod(np.scale, np.mod_f32, k8), np.mod_f32, a);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(1.0f, a[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[e] = 1.0f;
+            }
+            if (has_sh) {
+                unpack_mod(load_mod(np.shift, np.mod_f32, k8), np.mod_f32, b);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) b[e] = -0.0f;
+            }
+            s_mod[k8] = make_float4(a[0], a[1], a[2], a[3]);
+            s_mod[V + k8] = make_float4(a[4], a[5], a[6], a[7]);
+            s_mod[2 * V + k8] = make_float4(b[0], b[1], b[2], b[3]);
+            s_mod[3 * V + k8] = make_float4(b[4], b[5], b[6], b[7]);
+        }
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowsPerCta;
+        const int lane = static_cast<int>(threadIdx.x & 31);
+        int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+        uint4* buf = reinterpret_cast<uint4*>(s_mod + 4 * V) + (threadIdx.x >> 5) * V;
+        if (row < R) copy_row_async<NV, kFull>(A, row, K, buf, lane);
+        __syncthreads();
+        for (; row < R; row += stride)
+            norm_quant_row<kBf16Codes, NV, true, kFull, kNorm>(A, row, row + stride < R ? row + stride : -1, K, np,
+                                                               Q, S, lane, 32, s_mod, buf, red_sum, red_sq,
+                                                               red_max);
+    } else {
+        norm_quant_row<kBf16Codes, NV, false, false, kNorm>(A, static_cast<int64_t>(blockIdx.x), -1, K, np, Q, S,
+                                                            static_cast<int>(threadIdx.x),
+                                                            static_cast<int>(blockDim.x), s_mod, nullptr, red_sum,
+                                                            red_sq, red_max);
     }
 }
 

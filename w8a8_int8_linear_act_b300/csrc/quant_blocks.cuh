@@ -11,7 +11,7 @@
 // contiguous; the codes have the same shape and strides, the scales are
 // [B][H][ceil(L / block_tokens)].
 //
-// Structure.  One CTA per block.  A token's D elements are VD = D / E
+// Structure.  A CTA per block at a time.  A token's D elements are VD = D / E
 // 16-byte vectors; thread t takes vector t % VD of tokens t / VD, t / VD +
 // TPP, ... (TPP tokens per pass), so its column in the token is fixed and no
 // index is divided per vector, and every warp instruction covers whole
@@ -20,6 +20,8 @@
 // registers while its absmax is reduced (shuffles, then one shared-memory
 // step) and then quantised with the row quantiser's vector routine; blocks
 // too long for the registers are read twice (the second time from L2).
+// With the block in registers the CTAs are persistent and each thread's
+// vectors of the CTA's next block stream into shared memory meanwhile.
 #pragma once
 
 #include <cstdint>
@@ -42,51 +44,100 @@ struct BlockGeom {
 
 // Up to 8 vectors a thread: at most 64 registers, four 256-thread CTAs per
 // SM (79 registers gave three); 16 vectors keep their registers.
+//
+// NV > 0: persistent.  The grid holds the CTAs that fit on the GPU at once;
+// CTA c takes blocks c, c + gridDim.x, ...  Each thread copies its own
+// vectors of its next block into shared memory (cp.async, NV * blockDim.x
+// 16-byte slots of dynamic shared memory, slot i * blockDim.x + t for its
+// vector i) while it reduces and quantises the current one, so that HBM
+// keeps streaming during the arithmetic; no thread reads another's slots.
+// NV == 0: a CTA per block (gridDim.x == number of blocks).
 template <typename TIn, int NV>
 __global__ void __launch_bounds__(256, NV >= 16 ? 2 : 4) quant_blocks_kernel(const TIn* __restrict__ A, BlockGeom g,
-                                                           int8_t* __restrict__ Q, float* __restrict__ S)
+                                                                             int64_t nblocks, int8_t* __restrict__ Q,
+                                                                             float* __restrict__ S)
 {
     using IV = InVec<TIn>;
     constexpr int E = IV::kElems;
-    __shared__ float red[32];
+    // Two reduction arrays, used alternately by consecutive blocks of a CTA:
+    // a warp writing one for block n + 2 has passed block n + 1's barrier,
+    // which every warp reaches only after its last read of block n's.
+    __shared__ float red[2][32];
 
-    const int64_t blk = blockIdx.x;          // ((b * H) + h) * nblk + j
-    const int64_t j = blk % g.nblk;
-    const int64_t bh = blk / g.nblk;
-    const int64_t b = bh / g.H;
-    const int64_t h = bh - b * g.H;
-    const int64_t t0 = j * g.block_tokens;
-    const int ntok = static_cast<int>(min(g.block_tokens, g.L - t0));
     const int t = static_cast<int>(threadIdx.x);
     const bool active = t < g.tpp * g.vd;    // the CTA is rounded up to whole warps
     const int col = active ? t % g.vd : 0;
-    const int tok0 = active ? t / g.vd : ntok;
-    const int64_t base = b * g.stride_b + h * g.stride_h + t0 * g.stride_t + static_cast<int64_t>(col) * E;
+    const int tok0 = active ? t / g.vd : static_cast<int>(g.block_tokens);
     const int64_t step = static_cast<int64_t>(g.tpp) * g.stride_t;   // elements between a thread's vectors
 
-    uint32_t m2 = 0;
+    // Element offset of this thread's first vector in block blk, and the
+    // block's token count.  Block, head and block counts are below 2^31
+    // (checked by the host), so the index split runs in 32 bits.
+    auto locate = [&](int64_t blk, int& ntok) -> int64_t {
+        const uint32_t nb = static_cast<uint32_t>(g.nblk), hh = static_cast<uint32_t>(g.H);
+        const uint32_t bk = static_cast<uint32_t>(blk);   // blk = ((b * H) + h) * nblk + j
+        const uint32_t bh = bk / nb;
+        const uint32_t j = bk - bh * nb;
+        const uint32_t b = bh / hh;
+        const uint32_t h = bh - b * hh;
+        const int64_t t0 = static_cast<int64_t>(j) * g.block_tokens;
+        ntok = static_cast<int>(min(g.block_tokens, g.L - t0));
+        return static_cast<int64_t>(b) * g.stride_b + static_cast<int64_t>(h) * g.stride_h +
+               (t0 + tok0) * g.stride_t + static_cast<int64_t>(col) * E;
+    };
+
     if constexpr (NV > 0) {
-        uint4 v[NV];
-        const int64_t first = base + tok0 * g.stride_t;
+        extern __shared__ uint4 s_slots[];
+        const int T = static_cast<int>(blockDim.x);
+        auto copy_block = [&](int64_t first, int ntok) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
-            v[i] = tok0 + i * g.tpp < ntok ? load_stream(reinterpret_cast<const uint4*>(A + first + i * step))
-                                           : make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < NV; ++i)
+                if (tok0 + i * g.tpp < ntok) cp_async_16(&s_slots[i * T + t], A + first + i * step);
+            cp_async_commit();
+        };
+        int64_t blk = blockIdx.x;
+        int ntok = 0;
+        int64_t first = 0;
+        if (blk < nblocks) {
+            first = locate(blk, ntok);
+            copy_block(first, ntok);
+        }
+        for (int it = 0; blk < nblocks; blk += gridDim.x, ++it) {
+            cp_async_wait_all();
+            uint4 v[NV];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
-        const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red));
-        if (t == 0) S[blk] = rs.s;
+            for (int i = 0; i < NV; ++i) v[i] = tok0 + i * g.tpp < ntok ? s_slots[i * T + t] : make_uint4(0, 0, 0, 0);
+            uint32_t m2 = 0;
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (tok0 + i * g.tpp < ntok) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
+            for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
+            // Every v[i] has been read: the slots may take the next block.
+            int next_ntok = 0;
+            int64_t next_first = 0;
+            if (blk + gridDim.x < nblocks) {
+                next_first = locate(blk + gridDim.x, next_ntok);
+                copy_block(next_first, next_ntok);
+            }
+            const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red[it & 1]));
+            if (t == 0) S[blk] = rs.s;
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                if (tok0 + i * g.tpp < ntok) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
+            first = next_first;
+            ntok = next_ntok;
+        }
     } else {
+        const int64_t blk = blockIdx.x;
+        int ntok;
+        const int64_t base = locate(blk, ntok);
+        uint32_t m2 = 0;
         for (int tok = tok0; tok < ntok; tok += g.tpp)
-            IV::absmax(load_stream(reinterpret_cast<const uint4*>(A + base + tok * g.stride_t)), m2);
-        const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red));
+            IV::absmax(load_stream(reinterpret_cast<const uint4*>(A + base + (tok - tok0) * g.stride_t)), m2);
+        const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red[0]));
         if (t == 0) S[blk] = rs.s;
-        for (int tok = tok0; tok < ntok; tok += g.tpp)
-            quantize_vector<TIn, false>(*reinterpret_cast<const uint4*>(A + base + tok * g.stride_t), rs, Q,
-                                        base + tok * g.stride_t);
+        for (int tok = tok0; tok < ntok; tok += g.tpp) {
+            const int64_t off = base + (tok - tok0) * g.stride_t;
+            quantize_vector<TIn, false>(*reinterpret_cast<const uint4*>(A + off), rs, Q, off);
+        }
     }
 }
 

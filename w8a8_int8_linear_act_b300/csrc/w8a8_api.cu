@@ -812,33 +812,62 @@ HostPipe* host_pipe(int dev)
 
 // ---------------------------------------------------------------- norm + modulation + quant
 
-template <bool kBf16Codes, int NV, int kRows, int kNorm>
+template <bool kBf16Codes, int NV, int kRows, bool kFull, int kNorm>
 void launch_norm_cfg(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormParams& np, void* Q, float* S,
                      uint32_t* header, unsigned threads, cudaStream_t stream)
 {
-    const int64_t blocks = (M + kRows - 1) / kRows;
-    // The warp form stages the fp32 modulation in shared memory: 8 B per
-    // element of a row (32 KB at its largest, K = 4096).
-    const size_t smem = kRows > 1 ? static_cast<size_t>(K) * 8u : 0u;
-    w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kNorm>
+    int64_t blocks = (M + kRows - 1) / kRows;
+    // The warp form stages the fp32 modulation in shared memory, 8 B per
+    // element of a row, and a row buffer per warp, 2 B per element (96 KB at
+    // the largest, K = 4096, eight warps).
+    const size_t smem = kRows > 1 ? static_cast<size_t>(K) * (8u + 2u * kRows) : 0u;
+    if constexpr (kRows > 1) {
+        // Persistent warps: no more CTAs than fit on the GPU at once.
+        static std::once_flag attr_once;
+        std::call_once(attr_once, [] {
+            cudaFuncSetAttribute(w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kFull, kNorm>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 4096 * (8 + 2 * kRows));
+            cudaGetLastError();
+        });
+        const DeviceInfo* dev = device_info(nullptr);
+        int per_sm = 0;
+        if (dev != nullptr &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm, w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kFull, kNorm>, static_cast<int>(threads),
+                smem) == cudaSuccess &&
+            per_sm > 0) {
+            const int64_t resident = static_cast<int64_t>(per_sm) * dev->num_sms;
+            if (blocks > resident) blocks = resident;
+        }
+        cudaGetLastError();
+    }
+    w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kFull, kNorm>
         <<<static_cast<unsigned>(blocks), threads, smem, stream>>>(reinterpret_cast<const __nv_bfloat16*>(X), M, K,
                                                                    np, Q, S, header);
 }
 
 // Rows of up to 128 vectors: a warp per row with 4 vectors per lane; up to
 // 512: 16 per lane; up to 4096 (K <= 32768): a CTA per row, 16 per thread.
+// Rows of exactly 128, 256 or 512 vectors (K = 1024, 2048, 4096) take the
+// warp form with 4, 8 or 16 vectors per lane and no range checks.
 template <bool kBf16Codes, int kNorm>
 w8a8_status launch_norm_typed(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormParams& np, void* Q,
                               float* S, uint32_t* header, cudaStream_t stream)
 {
     const int64_t V = K / 8;
-    if (V <= 128)
-        launch_norm_cfg<kBf16Codes, 4, 4, kNorm>(X, M, K, np, Q, S, header, 128, stream);
+    if (V == 128)
+        launch_norm_cfg<kBf16Codes, 4, 8, true, kNorm>(X, M, K, np, Q, S, header, 256, stream);
+    else if (V == 256)
+        launch_norm_cfg<kBf16Codes, 8, 8, true, kNorm>(X, M, K, np, Q, S, header, 256, stream);
+    else if (V == 512)
+        launch_norm_cfg<kBf16Codes, 16, 8, true, kNorm>(X, M, K, np, Q, S, header, 256, stream);
+    else if (V <= 128)
+        launch_norm_cfg<kBf16Codes, 4, 8, false, kNorm>(X, M, K, np, Q, S, header, 256, stream);
     else if (V <= 512)
-        launch_norm_cfg<kBf16Codes, 16, 4, kNorm>(X, M, K, np, Q, S, header, 128, stream);
+        launch_norm_cfg<kBf16Codes, 16, 8, false, kNorm>(X, M, K, np, Q, S, header, 256, stream);
     else {
         const unsigned T = static_cast<unsigned>(((V + 15) / 16 + 31) / 32 * 32);
-        launch_norm_cfg<kBf16Codes, 16, 1, kNorm>(X, M, K, np, Q, S, header, T, stream);
+        launch_norm_cfg<kBf16Codes, 16, 1, false, kNorm>(X, M, K, np, Q, S, header, T, stream);
     }
     return last_launch_status();
 }
@@ -881,7 +910,30 @@ void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, i
                        cudaStream_t stream)
 {
     const unsigned threads = static_cast<unsigned>((g.tpp * g.vd + 31) / 32 * 32);
-    w8a8::quant_blocks_kernel<TIn, NV><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(X, g, Q, S);
+    // With the block in registers (NV > 0) the CTAs are persistent, each
+    // with NV 16-byte slots per thread for its next block: no more CTAs than
+    // fit on the GPU at once.
+    const size_t smem = NV > 0 ? static_cast<size_t>(NV) * threads * 16u : 0u;
+    int64_t grid = blocks;
+    if constexpr (NV > 0) {
+        static std::once_flag attr_once;
+        std::call_once(attr_once, [] {
+            cudaFuncSetAttribute(w8a8::quant_blocks_kernel<TIn, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 NV * kBlockThreads * 16);
+            cudaGetLastError();
+        });
+        const DeviceInfo* dev = device_info(nullptr);
+        int per_sm = 0;
+        if (dev != nullptr &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, w8a8::quant_blocks_kernel<TIn, NV>,
+                                                          static_cast<int>(threads), smem) == cudaSuccess &&
+            per_sm > 0) {
+            const int64_t resident = static_cast<int64_t>(per_sm) * dev->num_sms;
+            if (grid > resident) grid = resident;
+        }
+        cudaGetLastError();
+    }
+    w8a8::quant_blocks_kernel<TIn, NV><<<static_cast<unsigned>(grid), threads, smem, stream>>>(X, g, blocks, Q, S);
 }
 
 template <typename TIn>
