@@ -271,10 +271,22 @@ class ClockSampler:
             reasons = {n for n, v in zip(names, parts[3:]) if v.lower() == "active"}
             self.samples.append((time.perf_counter(), mhz, pw, reasons))
 
+    def _sample_now(self):
+        # One sample taken at once (NVML sources), so that a region shorter
+        # than the sampling period still holds its first and last instants.
+        if self._q is None:
+            return
+        try:
+            self.samples.append((time.perf_counter(), self._q.sm_clock(), self._q.power_w(), self._q.reasons()))
+        except Exception as e:
+            self.errors.append("sample: %s" % e)
+
     def mark(self, name):
         self.regions[name] = [time.perf_counter(), None]
+        self._sample_now()
 
     def end(self, name):
+        self._sample_now()
         self.regions[name][1] = time.perf_counter()
 
     def __exit__(self, *exc):
@@ -315,7 +327,8 @@ class ClockSampler:
     def summary(self):
         out = self._stats(self.samples, self.max_mhz)
         out["source"] = self.source
-        out["scope"] = "every 5 ms from before the warm-up to after the last GPU pass of this run"
+        out["scope"] = ("every 5 ms from before the warm-up to after the last GPU pass of this run, and at the "
+                        "start and end of each region")
         for name, (t0, t1) in self.regions.items():
             inside = [s for s in self.samples if t0 <= s[0] <= (t1 if t1 is not None else float("inf"))]
             st = self._stats(inside, self.max_mhz)
@@ -897,15 +910,18 @@ def run_ours(args):
         Xqk = torch.randn((1, heads, M, dh), generator=torch.Generator().manual_seed(77)).to(torch.bfloat16).to(dev)
         qk = {"shape": [1, heads, M, dh], "layout": "HND", "unit": "GB/s", "peak": pk["hbm_gbs"]}
         for qname, bt in (("query", 128), ("key", 64)):
-            q_ms = med(T.cold(lambda: w8.quantize_qk_blocks(Xqk, bt, stream=stream), PER_WORKLOAD_COLD))
-            qc_ms = T.cold_graph([lambda: w8.quantize_qk_blocks(Xqk, bt, stream=torch.cuda.current_stream())],
-                                 PER_WORKLOAD_COLD, clean=True)[0]
+            qe_ms = med(T.cold(lambda: w8.quantize_qk_blocks(Xqk, bt, stream=stream), PER_WORKLOAD_COLD))
+            call = [lambda: w8.quantize_qk_blocks(Xqk, bt, stream=torch.cuda.current_stream())]
+            q_ms = T.cold_graph(call, PER_WORKLOAD_COLD)[0]
+            qc_ms = T.cold_graph(call, PER_WORKLOAD_COLD, clean=True)[0]
             T.release()
             nbytes = Xqk.numel() * 3 + heads * (-(-M // bt)) * 4   # bf16 in, int8 out, one scale per block
             gbs = nbytes / (q_ms * 1e-3) / 1e9
-            qk[qname] = {"block_tokens": bt, "ms": q_ms, "achieved": gbs, "frac": gbs / qk["peak"],
-                         "algorithmic_bytes": nbytes,
+            qk[qname] = {"block_tokens": bt, "ms": q_ms, "ms_events": qe_ms, "achieved": gbs,
+                         "frac": gbs / qk["peak"], "algorithmic_bytes": nbytes,
                          "clean_l2": {"ms": qc_ms, "frac": nbytes / (qc_ms * 1e-3) / 1e9 / qk["peak"]}}
+        qk["timing"] = ("ms: graph replays of n x (flush, call) minus n x flush, per call; ms_events: median "
+                        "event interval around one call after a flush (adds the launch gap)")
         del Xqk
 
     # The norm + modulation prologue fused into the activation quantisation
@@ -932,10 +948,11 @@ def run_ours(args):
             ymod.copy_(Xd)
             w8.linear(ymod, Wp, sw, bd, out=Y, workspace=ws, stream=stream)
 
-        k_ms = med(T.cold(lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn, stream=stream), PER_WORKLOAD_COLD))
-        kc_ms = T.cold_graph([lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn,
-                                                           stream=torch.cuda.current_stream())],
-                             PER_WORKLOAD_COLD, clean=True)[0]
+        ke_ms = med(T.cold(lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn, stream=stream),
+                           PER_WORKLOAD_COLD))
+        call = [lambda: w8.norm_quantize_act(Xd, "rms", 1e-6, scn, shn, stream=torch.cuda.current_stream())]
+        k_ms = T.cold_graph(call, PER_WORKLOAD_COLD)[0]
+        kc_ms = T.cold_graph(call, PER_WORKLOAD_COLD, clean=True)[0]
         T.release()
         nl_ms = med(T.cold(lambda: w8.norm_linear(Xd, Wp, sw, bd, "rms", 1e-6, scn, shn, out=Y, workspace=ws,
                                                   stream=stream), PER_WORKLOAD_COLD))
@@ -943,6 +960,7 @@ def run_ours(args):
         um_ms = med(T.cold(unfused_min, PER_WORKLOAD_COLD))
         nbytes = M * K * 2 + M * K + M * 4 + 2 * K * 2
         normp = {"kernel": "norm_quant_rows_kernel (RMS norm, bf16 modulation, int8 codes)", "ms": k_ms,
+                 "ms_events": ke_ms,
                  "achieved": nbytes / (k_ms * 1e-3) / 1e9, "unit": "GB/s", "peak": pk["hbm_gbs"],
                  "frac": nbytes / (k_ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
                  "clean_l2": {"ms": kc_ms, "frac": nbytes / (kc_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
@@ -950,9 +968,10 @@ def run_ours(args):
                  "unfused_torch_norm_then_linear_ms": un_ms,
                  "unfused_copy_then_linear_ms": um_ms,
                  "linear_step_ms": med(s_ms),
-                 "note": "medians, L2 flushed; unfused_torch: PyTorch rms_norm x (1 + scale) + shift written as bf16, "
-                         "then w8a8_linear; unfused_copy: a bf16 copy of X then w8a8_linear (a floor for any "
-                         "separate norm kernel)"}
+                 "note": "L2 flushed; ms: graph replays of n x (flush, call) minus n x flush, per call; the "
+                         "rest: medians of event intervals; unfused_torch: PyTorch rms_norm x (1 + scale) + shift "
+                         "written as bf16, then w8a8_linear; unfused_copy: a bf16 copy of X then w8a8_linear (a "
+                         "floor for any separate norm kernel)"}
         del ymod
 
     # The MLP pair at the MLP workload's sizes (6144 x 4096 -> 16384 -> 4096):

@@ -40,6 +40,8 @@ def check(X, bt, layout, dev):
     ((1, 2, 300, 128), 1, "HND"),       # one token per block
     ((1, 1, 4096, 128), 4096, "HND"),   # one block longer than the registers hold: read twice
     ((1, 2, 40, 2048), 8, "HND"),       # D = 2048: a token is 256 vectors
+    ((2, 300, 3, 128), 128, "NHD"),     # 512-thread CTAs, ragged last block
+    ((1, 2, 600, 128), 256, "HND"),     # 4096-vector blocks: 256 threads of 16 vectors
 ])
 def test_qk_blocks_bf16(cuda_device, shape, bt, layout):
     check(make(shape, seed=sum(shape) + bt, outlier_tokens=3), bt, layout, cuda_device)

@@ -15,8 +15,10 @@
 // 16-byte vectors; thread t takes vector t % VD of tokens t / VD, t / VD +
 // TPP, ... (TPP tokens per pass), so its column in the token is fixed and no
 // index is divided per vector, and every warp instruction covers whole
-// 16-byte vectors of neighbouring tokens.  A CTA has up to 256 threads (a
-// 128-token block of D = 128: 8 vectors per thread).  The block is held in
+// 16-byte vectors of neighbouring tokens.  A CTA has up to 256 threads, or
+// 512 for blocks of 2048 vectors or more (a 128-token block of D = 128: 512
+// threads of 4 vectors), so that a persistent CTA works through more,
+// smaller blocks' worth of copies.  The block is held in
 // registers while its absmax is reduced (shuffles, then one shared-memory
 // step) and then quantised with the row quantiser's vector routine; blocks
 // too long for the registers are read twice (the second time from L2).
@@ -42,8 +44,9 @@ struct BlockGeom {
     int32_t tpp;           // tokens per pass, 1 <= tpp * vd <= 256
 };
 
-// Up to 8 vectors a thread: at most 64 registers, four 256-thread CTAs per
-// SM (79 registers gave three); 16 vectors keep their registers.
+// Up to 8 vectors a thread: at most 64 registers, 1024 threads per SM (79
+// registers gave 768); 16 vectors keep their registers.  CTAs of up to 512
+// threads take up to 4 vectors a thread, 256 threads more.
 //
 // NV > 0: persistent.  The grid holds the CTAs that fit on the GPU at once;
 // CTA c takes blocks c, c + gridDim.x, ...  Each thread copies its own
@@ -53,7 +56,7 @@ struct BlockGeom {
 // keeps streaming during the arithmetic; no thread reads another's slots.
 // NV == 0: a CTA per block (gridDim.x == number of blocks).
 template <typename TIn, int NV>
-__global__ void __launch_bounds__(256, NV >= 16 ? 2 : 4) quant_blocks_kernel(const TIn* __restrict__ A, BlockGeom g,
+__global__ void __launch_bounds__(NV >= 8 ? 256 : 512, NV >= 16 ? 2 : (NV >= 8 ? 4 : 2)) quant_blocks_kernel(const TIn* __restrict__ A, BlockGeom g,
                                                                              int64_t nblocks, int8_t* __restrict__ Q,
                                                                              float* __restrict__ S)
 {
@@ -120,8 +123,15 @@ __global__ void __launch_bounds__(256, NV >= 16 ? 2 : 4) quant_blocks_kernel(con
             const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red[it & 1]));
             if (t == 0) S[blk] = rs.s;
 #pragma unroll
-            for (int i = 0; i < NV; ++i)
-                if (tok0 + i * g.tpp < ntok) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
+            for (int i = 0; i < NV; ++i) {
+                const bool valid = tok0 + i * g.tpp < ntok;
+                if constexpr (E == 8) {
+                    // every lane of the CTA comes here together
+                    quantize_vector_x2<false, true>(v[i], rs, Q, first + i * step, valid);
+                } else {
+                    if (valid) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
+                }
+            }
             first = next_first;
             ntok = next_ntok;
         }

@@ -230,6 +230,110 @@ __device__ __forceinline__ void quantize_vector(const uint4& vec, const RowScale
         store_codes<false, E>(Q, off, t);
 }
 
+// Two independent fp32 operations in one instruction (sm_100 and later);
+// each half is rounded exactly as the scalar operation would round it, so
+// the packed forms change no result, only the instruction count.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Both bf16 of a 32-bit word as fp32 (low half first).
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// quantize_vector on one vector of bf16, in packed pairs: t = fma(x, r, M),
+// the residual fma(x, r, M - t) and its check, with the same scalar
+// fallback by division near a tie.  kWarpUniform: all 32 lanes of the warp
+// call this together, so the rare near-tie branch is taken by the whole
+// warp or by none (one vote, no divergence bookkeeping); lanes with `valid`
+// false compute but neither take the fallback nor store.
+template <bool kBf16Codes, bool kWarpUniform>
+__device__ __forceinline__ void quantize_vector_x2(const uint4& vec, const RowScale& rs, void* Q, int64_t off,
+                                                   bool valid = true)
+{
+    const uint32_t w[4] = {vec.x, vec.y, vec.z, vec.w};
+    const float2 rr = make_float2(rs.r, rs.r), mm = make_float2(kRoundMagic, kRoundMagic);
+    float t[8], nq[8];
+    float dmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 x = bf16x2_to_f2(w[i]);
+        const float2 tt = fma2(x, rr, mm);
+        const float2 n = sub2(mm, tt);           // minus the code, exactly
+        const float2 res = fma2(x, rr, n);
+        dmax = fmaxf(dmax, fmaxf(fabsf(res.x), fabsf(res.y)));
+        t[2 * i] = tt.x;
+        t[2 * i + 1] = tt.y;
+        nq[2 * i] = n.x;
+        nq[2 * i + 1] = n.y;
+    }
+    const bool slow = valid && (dmax > kNearHalf || rs.exact);
+    if (kWarpUniform ? __any_sync(0xFFFFFFFFu, slow) : slow) {
+        float x[8];
+        InVec<__nv_bfloat16>::unpack(vec, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (rs.exact || fabsf(__fmaf_rn(x[e], rs.r, nq[e])) > kNearHalf)
+                t[e] = __fadd_rn(code_by_division(x[e], rs.s), kRoundMagic);
+    }
+    if (!valid) return;
+    if constexpr (kBf16Codes) {
+        // q = t - M, as the scalar form computes it (+0 for a zero code).
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 qq = sub2(make_float2(t[2 * i], t[2 * i + 1]), mm);
+            q[2 * i] = qq.x;
+            q[2 * i + 1] = qq.y;
+        }
+        store_codes<true, 8>(Q, off, q);
+    } else {
+        store_codes<false, 8>(Q, off, t);
+    }
+}
+
 // Rows of A [R][K] -> codes Q [R][K] and scales S [R].
 //   kRowsPerCta > 0: blockDim.x == 32 * kRowsPerCta, warp w takes row
 //                    blockIdx.x * kRowsPerCta + w (rows past R do nothing);

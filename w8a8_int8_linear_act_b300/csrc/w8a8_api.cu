@@ -903,7 +903,9 @@ w8a8_status check_norm_args(const uint16_t* X, int64_t M, int64_t K, int norm, f
 
 // ---------------------------------------------------------------- Query/Key blocks
 
-constexpr int kBlockThreads = 256;   // threads per CTA of the Query/Key block quantiser, at most
+constexpr int kBlockThreads = 256;   // threads per CTA of the Query/Key block quantiser, at most,
+constexpr int kBlockThreadsWide = 512;   // or for blocks of kWideBlockVectors vectors or more
+constexpr int64_t kWideBlockVectors = 2048;
 
 template <typename TIn, int NV>
 void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, int8_t* Q, float* S,
@@ -919,7 +921,7 @@ void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, i
         static std::once_flag attr_once;
         std::call_once(attr_once, [] {
             cudaFuncSetAttribute(w8a8::quant_blocks_kernel<TIn, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 NV * kBlockThreads * 16);
+                                 NV * (NV >= 8 ? kBlockThreads : kBlockThreadsWide) * 16);
             cudaGetLastError();
         });
         const DeviceInfo* dev = device_info(nullptr);
@@ -1291,8 +1293,13 @@ w8a8_status w8a8_quantize_qk_blocks(const void* X, int x_dtype, int64_t B, int64
     g.vd = static_cast<int32_t>(D / E);
     // Tokens per pass: as many as 256 threads cover (more warps per SM; a
     // form with up to 16 vectors per thread and fewer threads measured
-    // slower at the video attention shape).
-    const int64_t cap = kBlockThreads / g.vd;
+    // slower at the video attention shape), or 512 threads for blocks of
+    // 2048 vectors or more that then take at most 4 vectors a thread (the
+    // persistent CTAs work through twice as many blocks, overlapping more of
+    // the copies).
+    int64_t cap = kBlockThreads / g.vd;
+    const int64_t wide = kBlockThreadsWide / g.vd;
+    if (g.vd * g.block_tokens >= kWideBlockVectors && (g.block_tokens + wide - 1) / wide <= 4) cap = wide;
     g.tpp = static_cast<int32_t>(cap < g.block_tokens ? cap : g.block_tokens);
     if (layout == W8A8_LAYOUT_HND) {
         g.stride_t = D;
