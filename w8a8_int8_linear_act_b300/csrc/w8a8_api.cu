@@ -488,11 +488,16 @@ void launch_quant_cfg(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uin
 // threads per row reading it twice.
 constexpr int kQuantRows = 4;
 
-// Fewer rows than this many per SM: a CTA per row of at most 256 threads with
-// 2, 4 or 8 vectors a thread (rows of 64 to 2048 vectors), so that the few
-// rows spread over the SMs instead of filling a handful of them a warp per
-// row.
-constexpr int64_t kFewRowsPerSm = 2;
+// Up to this many rows per SM: a CTA per row of at most 256 threads with 2,
+// 4 or 8 vectors a thread (rows of 64 to 2048 vectors).  A warp per row
+// walks its row's vectors one after another, and with few warps per SM that
+// serial chain, not HBM, sets the time (297 rows of 4096: 15.1 µs against
+// 4.5 µs with a CTA per row).  Measured on B300 with L2 flushed, the CTA per
+// row is as fast or faster up to 6144 rows for rows of 128 to 512 vectors
+// (6144 x 4096 with outlier columns: 21.3 against 22.5 µs; 1001 x 2048:
+// 4.6 against 8.9 µs), the warp per row from about 9500 rows on (28672 x
+// 4096: 75.0 against 85.3 µs).
+constexpr int64_t kFewRowsPerSm = 48;
 
 template <typename TIn, bool kBf16Codes>
 w8a8_status launch_quant_typed(const TIn* A, int64_t R, int64_t K, void* Q, float* S, uint32_t* header,
