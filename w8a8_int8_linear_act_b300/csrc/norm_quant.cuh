@@ -268,11 +268,19 @@ __device__ __forceinline__ void norm_quant_row(const __nv_bfloat16* __restrict__
     const float amax = kWarp ? warp_max(IV::absmax_value(m2)) : block_max(IV::absmax_value(m2), red_max);
     const RowScale rs = row_scale(amax);
     if (t == 0) S[row] = rs.s;
+    if (rs.corr) {
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int idx = t + i * T;
-        if (kFull || idx < V)
-            quantize_vector_x2<kBf16Codes, kFull>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+        for (int i = 0; i < NV; ++i) {
+            const int idx = t + i * T;
+            if (kFull || idx < V) quantize_vector_corr<kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int idx = t + i * T;
+            if (kFull || idx < V)
+                quantize_vector<__nv_bfloat16, kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+        }
     }
 }
 

@@ -122,15 +122,14 @@ __global__ void __launch_bounds__(NV >= 8 ? 256 : 512, NV >= 16 ? 2 : (NV >= 8 ?
             }
             const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red[it & 1]));
             if (t == 0) S[blk] = rs.s;
+            if (E == 8 && rs.corr) {
 #pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const bool valid = tok0 + i * g.tpp < ntok;
-                if constexpr (E == 8) {
-                    // every lane of the CTA comes here together
-                    quantize_vector_x2<false, true>(v[i], rs, Q, first + i * step, valid);
-                } else {
-                    if (valid) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
-                }
+                for (int i = 0; i < NV; ++i)
+                    if (tok0 + i * g.tpp < ntok) quantize_vector_corr<false>(v[i], rs, Q, first + i * step);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NV; ++i)
+                    if (tok0 + i * g.tpp < ntok) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
             }
             first = next_first;
             ntok = next_ntok;
@@ -146,7 +145,10 @@ __global__ void __launch_bounds__(NV >= 8 ? 256 : 512, NV >= 16 ? 2 : (NV >= 8 ?
         if (t == 0) S[blk] = rs.s;
         for (int tok = tok0; tok < ntok; tok += g.tpp) {
             const int64_t off = base + (tok - tok0) * g.stride_t;
-            quantize_vector<TIn, false>(*reinterpret_cast<const uint4*>(A + off), rs, Q, off);
+            if (E == 8 && rs.corr)
+                quantize_vector_corr<false>(*reinterpret_cast<const uint4*>(A + off), rs, Q, off);
+            else
+                quantize_vector<TIn, false>(*reinterpret_cast<const uint4*>(A + off), rs, Q, off);
         }
     }
 }

@@ -32,9 +32,15 @@
 // to a tie (about one in 8000 for smooth data), and rows whose reciprocal
 // overflows (s below 2^-128), take the IEEE division.  The test is made
 // once per 16-byte vector (the largest |d| of its elements), and the
-// division sits behind that one branch in an out-of-line function, so the
-// common path pays no part of it.  In the fast path |p| <= 127 * (1 + 2^-22),
-// so no clamp is needed there.
+// division sits behind that one branch in an out-of-line function.  In the
+// fast path |p| <= 127 * (1 + 2^-22), so no clamp is needed there.
+//
+// bf16 inputs take neither the test nor the division (quantize_vector_corr):
+// one more fused multiply-add turns fp32(x r) into the correctly rounded
+// quotient fp32(x / s) itself (Markstein's correction step), and that rounds
+// to the code directly.  bf16 data with a round absmax puts many elements
+// exactly on a tie of x r (0.3 % of a Gaussian Query tensor), where the test
+// above would send most vectors to the division; fp32 inputs keep the test.
 #pragma once
 
 #include <cstdint>
@@ -105,6 +111,7 @@ struct RowScale {
     float s;        // scale (1 for a zero row)
     float r;        // fp32(1 / s)
     bool exact;     // reciprocal overflowed: every element takes the division
+    bool corr;      // bf16 elements may take quantize_vector_corr (s >= 2^-100, r finite)
 };
 
 // A zero row (amax / 127 == 0, including an fp32 amax that underflows) gets
@@ -116,6 +123,7 @@ __device__ __forceinline__ RowScale row_scale(float amax)
     rs.s = (s == 0.0f) ? 1.0f : s;
     rs.r = __frcp_rn(rs.s);
     rs.exact = !(fabsf(rs.r) <= 3.402823466e38f);
+    rs.corr = !rs.exact && rs.s >= 7.888609052210118e-31f;   // 2^-100
     return rs;
 }
 
@@ -283,44 +291,43 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// quantize_vector on one vector of bf16, in packed pairs: t = fma(x, r, M),
-// the residual fma(x, r, M - t) and its check, with the same scalar
-// fallback by division near a tie.  kWarpUniform: all 32 lanes of the warp
-// call this together, so the rare near-tie branch is taken by the whole
-// warp or by none (one vote, no divergence bookkeeping); lanes with `valid`
-// false compute but neither take the fallback nor store.
-template <bool kBf16Codes, bool kWarpUniform>
-__device__ __forceinline__ void quantize_vector_x2(const uint4& vec, const RowScale& rs, void* Q, int64_t off,
-                                                   bool valid = true)
+// Codes of one vector of bf16, without a tie test or a division, for a row
+// with rs.corr.  Per element, in packed pairs of fp32:
+//   q0  = fp32(x r)
+//   rem = fma(-q0, s, x)      the remainder x - q0 s, exact
+//   q1  = fma(rem, r, q0)     = fp32(x / s), the correctly rounded quotient
+//   t   = q1 + 1.5 2^23       rounds q1 to an integer, half to even
+// The last FMA is Markstein's correction step (P. Markstein, IBM J. Res.
+// Dev. 34(1), 1990; the FMA-based division theorems in Muller et al.,
+// Handbook of Floating-Point Arithmetic, ch. 5): with r the correctly rounded
+// reciprocal it yields the correctly rounded quotient, so rounding q1 to an
+// integer gives exactly round_half_even(fp32(x / s)) -- the codes of the
+// division form, ties included, which the fast path of quantize_vector has
+// to refer to the division.  For bf16 x and s = fp32(amax / 127) with amax
+// bf16 this was checked against exact rational arithmetic for every pair of
+// significands and 40 binary orders of magnitude of x below amax, both
+// signs; the steps scale exactly by powers of two, which covers every row
+// whose values stay normal (s >= 2^-100; other rows use quantize_vector).
+// |fp32(x / s)| <= 127 (1 + 2^-23) here, so no clamp is needed.
+template <bool kBf16Codes>
+__device__ __forceinline__ void quantize_vector_corr(const uint4& vec, const RowScale& rs, void* Q, int64_t off)
 {
     const uint32_t w[4] = {vec.x, vec.y, vec.z, vec.w};
-    const float2 rr = make_float2(rs.r, rs.r), mm = make_float2(kRoundMagic, kRoundMagic);
-    float t[8], nq[8];
-    float dmax = 0.0f;
+    const float2 rr = make_float2(rs.r, rs.r), ns = make_float2(-rs.s, -rs.s);
+    const float2 mm = make_float2(kRoundMagic, kRoundMagic);
+    float t[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float2 x = bf16x2_to_f2(w[i]);
-        const float2 tt = fma2(x, rr, mm);
-        const float2 n = sub2(mm, tt);           // minus the code, exactly
-        const float2 res = fma2(x, rr, n);
-        dmax = fmaxf(dmax, fmaxf(fabsf(res.x), fabsf(res.y)));
+        const float2 q0 = mul2(x, rr);
+        const float2 rem = fma2(q0, ns, x);
+        const float2 q1 = fma2(rem, rr, q0);
+        const float2 tt = add2(q1, mm);
         t[2 * i] = tt.x;
         t[2 * i + 1] = tt.y;
-        nq[2 * i] = n.x;
-        nq[2 * i + 1] = n.y;
     }
-    const bool slow = valid && (dmax > kNearHalf || rs.exact);
-    if (kWarpUniform ? __any_sync(0xFFFFFFFFu, slow) : slow) {
-        float x[8];
-        InVec<__nv_bfloat16>::unpack(vec, x);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (rs.exact || fabsf(__fmaf_rn(x[e], rs.r, nq[e])) > kNearHalf)
-                t[e] = __fadd_rn(code_by_division(x[e], rs.s), kRoundMagic);
-    }
-    if (!valid) return;
     if constexpr (kBf16Codes) {
-        // q = t - M, as the scalar form computes it (+0 for a zero code).
+        // q = t - M, +0 for a zero code.
         float q[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -390,10 +397,18 @@ __global__ void __launch_bounds__(kRowsPerCta > 0 ? 32 * kRowsPerCta : (NV > 0 ?
             S[row] = rs.s;
             if (zero_rows != nullptr) zero_rows[row] = 0u;
         }
+        if (E == 8 && rs.corr) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int idx = t + i * T;
-            if (idx < V) quantize_vector<TIn, kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+            for (int i = 0; i < NV; ++i) {
+                const int idx = t + i * T;
+                if (idx < V) quantize_vector_corr<kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int idx = t + i * T;
+                if (idx < V) quantize_vector<TIn, kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+            }
         }
     } else {
         for (int idx = t; idx < V; idx += T) IV::absmax(load_stream(src + idx), m2);
@@ -403,8 +418,12 @@ __global__ void __launch_bounds__(kRowsPerCta > 0 ? 32 * kRowsPerCta : (NV > 0 ?
             S[row] = rs.s;
             if (zero_rows != nullptr) zero_rows[row] = 0u;
         }
-        for (int idx = t; idx < V; idx += T)
-            quantize_vector<TIn, kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+        for (int idx = t; idx < V; idx += T) {
+            if (E == 8 && rs.corr)
+                quantize_vector_corr<kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+            else
+                quantize_vector<TIn, kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+        }
     }
 }
 
@@ -434,11 +453,19 @@ __global__ void __launch_bounds__(256) codes_known_amax_kernel(const __nv_bfloat
             const int idx = base + u * static_cast<int>(blockDim.x);
             v[u] = idx < V ? load_stream(src + idx) : make_uint4(0, 0, 0, 0);
         }
+        if (rs.corr) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int idx = base + u * static_cast<int>(blockDim.x);
-            if (idx < V)
-                quantize_vector<__nv_bfloat16, kBf16Codes>(v[u], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+            for (int u = 0; u < kU; ++u) {
+                const int idx = base + u * static_cast<int>(blockDim.x);
+                if (idx < V) quantize_vector_corr<kBf16Codes>(v[u], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int idx = base + u * static_cast<int>(blockDim.x);
+                if (idx < V)
+                    quantize_vector<__nv_bfloat16, kBf16Codes>(v[u], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
+            }
         }
     }
 }
