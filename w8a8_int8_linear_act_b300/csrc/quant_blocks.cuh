@@ -122,10 +122,15 @@ __global__ void __launch_bounds__(NV >= 8 ? 256 : 512, NV >= 16 ? 2 : (NV >= 8 ?
             }
             const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red[it & 1]));
             if (t == 0) S[blk] = rs.s;
-            if (E == 8 && rs.corr) {
+            if constexpr (E == 8) {
+                if (rs.corr) {
 #pragma unroll
-                for (int i = 0; i < NV; ++i)
-                    if (tok0 + i * g.tpp < ntok) quantize_vector_corr<false>(v[i], rs, Q, first + i * step);
+                    for (int i = 0; i < NV; ++i)
+                        if (tok0 + i * g.tpp < ntok) quantize_vector_corr<false>(v[i], rs, Q, first + i * step);
+                } else if (tok0 < ntok) {
+                    quantize_strided_by_tie_test<TIn, false>(A, first, step, (ntok - tok0 + g.tpp - 1) / g.tpp, rs,
+                                                             Q);
+                }
             } else {
 #pragma unroll
                 for (int i = 0; i < NV; ++i)

@@ -341,6 +341,21 @@ __device__ __forceinline__ void quantize_vector_corr(const uint4& vec, const Row
     }
 }
 
+// Codes, by quantize_vector, of `count` 16-byte vectors of A at element
+// offsets base, base + stride, ... (the codes at the same offsets of Q).  For
+// the rare bf16 rows without rs.corr (scales below 2^-100, or a reciprocal
+// that overflows): out of line and reading the vectors again from memory, so
+// that the common path keeps neither its registers nor its code.
+template <typename TIn, bool kBf16Codes>
+__device__ __noinline__ void quantize_strided_by_tie_test(const TIn* __restrict__ A, int64_t base, int64_t stride,
+                                                          int count, RowScale rs, void* __restrict__ Q)
+{
+    for (int j = 0; j < count; ++j) {
+        const int64_t off = base + j * stride;
+        quantize_vector<TIn, kBf16Codes>(*reinterpret_cast<const uint4*>(A + off), rs, Q, off);
+    }
+}
+
 // Rows of A [R][K] -> codes Q [R][K] and scales S [R].
 //   kRowsPerCta > 0: blockDim.x == 32 * kRowsPerCta, warp w takes row
 //                    blockIdx.x * kRowsPerCta + w (rows past R do nothing);
@@ -356,7 +371,8 @@ constexpr int kQuantWarpsPerSm = 21;
 
 template <typename TIn, bool kBf16Codes, int NV, int kRowsPerCta>
 __global__ void __launch_bounds__(kRowsPerCta > 0 ? 32 * kRowsPerCta : (NV > 0 ? 256 : 1024),
-                                  kRowsPerCta > 0 ? kQuantWarpsPerSm / (kRowsPerCta > 0 ? kRowsPerCta : 1) : 1)
+                                  kRowsPerCta > 0 ? kQuantWarpsPerSm / (kRowsPerCta > 0 ? kRowsPerCta : 1)
+                                                  : (NV > 0 && NV <= 2 ? 8 : 1))
     quant_rows_kernel(const TIn* __restrict__ A, int64_t R, int64_t K,
                                                           void* __restrict__ Q, float* __restrict__ S,
                                                           uint32_t* __restrict__ header,
@@ -397,11 +413,17 @@ __global__ void __launch_bounds__(kRowsPerCta > 0 ? 32 * kRowsPerCta : (NV > 0 ?
             S[row] = rs.s;
             if (zero_rows != nullptr) zero_rows[row] = 0u;
         }
-        if (E == 8 && rs.corr) {
+        if constexpr (E == 8) {
+            if (rs.corr) {
 #pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int idx = t + i * T;
-                if (idx < V) quantize_vector_corr<kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+                for (int i = 0; i < NV; ++i) {
+                    const int idx = t + i * T;
+                    if (idx < V)
+                        quantize_vector_corr<kBf16Codes>(v[i], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+                }
+            } else if (t < V) {
+                quantize_strided_by_tie_test<TIn, kBf16Codes>(A, out0 + static_cast<int64_t>(t) * E,
+                                                              static_cast<int64_t>(T) * E, (V - t + T - 1) / T, rs, Q);
             }
         } else {
 #pragma unroll
@@ -418,11 +440,12 @@ __global__ void __launch_bounds__(kRowsPerCta > 0 ? 32 * kRowsPerCta : (NV > 0 ?
             S[row] = rs.s;
             if (zero_rows != nullptr) zero_rows[row] = 0u;
         }
-        for (int idx = t; idx < V; idx += T) {
-            if (E == 8 && rs.corr)
+        if (E == 8 && rs.corr) {
+            for (int idx = t; idx < V; idx += T)
                 quantize_vector_corr<kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
-            else
-                quantize_vector<TIn, kBf16Codes>(src[idx], rs, Q, out0 + static_cast<int64_t>(idx) * E);
+        } else if (t < V) {
+            quantize_strided_by_tie_test<TIn, kBf16Codes>(A, out0 + static_cast<int64_t>(t) * E,
+                                                          static_cast<int64_t>(T) * E, (V - t + T - 1) / T, rs, Q);
         }
     }
 }
@@ -460,12 +483,10 @@ __global__ void __launch_bounds__(256) codes_known_amax_kernel(const __nv_bfloat
                 if (idx < V) quantize_vector_corr<kBf16Codes>(v[u], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
             }
         } else {
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int idx = base + u * static_cast<int>(blockDim.x);
-                if (idx < V)
-                    quantize_vector<__nv_bfloat16, kBf16Codes>(v[u], rs, Q, out0 + static_cast<int64_t>(idx) * 8);
-            }
+            const int n = (V - base + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+            quantize_strided_by_tie_test<__nv_bfloat16, kBf16Codes>(A, out0 + static_cast<int64_t>(base) * 8,
+                                                                    static_cast<int64_t>(blockDim.x) * 8,
+                                                                    n < kU ? n : kU, rs, Q);
         }
     }
 }
