@@ -491,6 +491,16 @@ __global__ void __launch_bounds__(256) codes_known_amax_kernel(const __nv_bfloat
     }
 }
 
+// Clears the workspace header (status word and split-tile counters) for a
+// GEMM that no quantiser precedes (the BF16 linear).  It releases its
+// dependents at entry, so the GEMM, launched as its programmatic dependent,
+// runs its set-up meanwhile and waits on the device for these stores.
+__global__ void __launch_bounds__(256) clear_header_kernel(uint32_t* __restrict__ header)
+{
+    grid_launch_dependents();
+    for (int i = threadIdx.x; i < kHeaderWords; i += blockDim.x) header[i] = 0u;
+}
+
 // int8 codes -> the same integers as bf16 (exact), 16 codes per thread step.
 // `header`, when not NULL, is the workspace header, cleared by block 0.
 __global__ void codes_to_bf16_kernel(const int8_t* __restrict__ Qi, uint16_t* __restrict__ Qb, int64_t n16,

@@ -1269,11 +1269,11 @@ w8a8_status w8a8_bf16_linear(const uint16_t* X, int64_t M, int64_t K, const uint
     if (!dev) return W8A8_ERR_NO_DEVICE;
     uint8_t* w = ws_base(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // No quantiser runs first to clear the header: clear it here.
-    if (cudaMemsetAsync(w + L.status_off, 0, kAlign, s) != cudaSuccess) {
-        cudaGetLastError();
-        return W8A8_ERR_CUDA;
-    }
+    // No quantiser runs first to clear the header: a one-CTA kernel does,
+    // with the GEMM as its programmatic dependent.
+    static_assert(w8a8::kHeaderWords * 4 == kAlign, "the header is one alignment unit");
+    w8a8::clear_header_kernel<<<1, 256, 0, s>>>(reinterpret_cast<uint32_t*>(w + L.status_off));
+    if (cudaGetLastError() != cudaSuccess) return W8A8_ERR_CUDA;
     const int bias_mode = bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0;
     return launch_gemm<w8a8::kModeBf16>(dev, X, W, M, N, K, nullptr, nullptr, bias, bias_mode, Y, w, L,
                                         ws_slots(L, ws_bytes), s);
