@@ -141,6 +141,19 @@ def test_norm_quant_zero_and_constant_rows(cuda_device):
     assert float(sx[5]) == 1.0 and not Xq[5].any() and float(sx[2]) == 1.0
 
 
+@pytest.mark.parametrize("e", [-100, -101, -110])
+def test_norm_quant_tiny_shift_rows(cuda_device, e):
+    """Zero rows under RMS norm become y = shift exactly; with a shift of
+    absmax 127 * 2^e their scale lies around 2^-100, where the codes switch
+    from the division-free correction step to the tie test with IEEE
+    division.  Checked like every other row (bit-exact outside the band)."""
+    X = torch.randn(6, 1024, generator=torch.Generator().manual_seed(11)).to(torch.bfloat16)
+    X[1:5] = 0.0
+    sh = torch.randn(1024, generator=torch.Generator().manual_seed(12), dtype=torch.float64)
+    sh = (sh / sh.abs().max() * 127.0 * 2.0 ** e).to(torch.float32)
+    check(X, "rms", 1e-6, None, sh, cuda_device)
+
+
 def test_norm_linear_is_linear_of_the_modulated_rows(cuda_device):
     """w8a8_norm_linear equals w8a8_linear applied to the prologue's own y,
     bit for bit (the GEMM half is the parity-tested linear)."""

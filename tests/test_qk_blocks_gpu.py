@@ -47,6 +47,25 @@ def test_qk_blocks_bf16(cuda_device, shape, bt, layout):
     check(make(shape, seed=sum(shape) + bt, outlier_tokens=3), bt, layout, cuda_device)
 
 
+@pytest.mark.parametrize("shape,bt,layout", [
+    ((1, 8, 1024, 128), 128, "HND"),   # 512-thread CTAs of 4 vectors
+    ((1, 8, 1024, 128), 256, "HND"),   # 256 threads of 16 vectors
+    ((1, 6, 300, 64), 64, "NHD"),      # ragged last blocks
+])
+def test_qk_blocks_tiny_scales(cuda_device, shape, bt, layout):
+    """Blocks whose scale lies on either side of 2^-100 (the correction step
+    against the out-of-line tie test with division), bit-exact."""
+    X = make(shape, seed=sum(shape) + bt).to(torch.float32)
+    tok_axis = 2 if layout == "HND" else 1
+    L = shape[tok_axis]
+    exps = [0, -100, -101, -110, -126, 15]
+    for j, t0 in enumerate(range(0, L, bt)):
+        sl = [slice(None)] * 4
+        sl[tok_axis] = slice(t0, t0 + bt)
+        X[tuple(sl)] *= 2.0 ** exps[j % len(exps)]
+    check(X.to(torch.bfloat16), bt, layout, cuda_device)
+
+
 def test_qk_blocks_fp32_and_zero_block(cuda_device):
     X = make((1, 4, 200, 64), seed=5, dtype=torch.float32)
     X[0, 2, 64:128] = 0.0

@@ -92,6 +92,29 @@ def test_zero_and_denormal_rows(cuda_device):
     check_rows(Xb, cuda_device)
 
 
+def scaled_rows(M, K, exps, seed):
+    """bf16 rows of Gaussian values scaled to absmax 127 * 2^e for the given
+    exponents (cycled), with exact ties and a lossless code sprinkled in."""
+    g = torch.Generator().manual_seed(seed)
+    X = torch.randn(M, K, generator=g, dtype=torch.float64)
+    X = X / X.abs().amax(dim=1, keepdim=True) * 127.0
+    X[:, 1] = 127.0
+    X[:, 2:34] = torch.arange(32, dtype=torch.float64) - 15.5   # exact half-integers of s
+    for i in range(M):
+        X[i] *= 2.0 ** exps[i % len(exps)]
+    return X.to(torch.float32).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("M,K", [(8, 4096), (8, 1024), (7300, 512)])
+def test_tiny_scales_both_code_paths(cuda_device, M, K):
+    """bf16 rows whose scale lies on either side of 2^-100, where the kernels
+    switch from the division-free correction step to the out-of-line tie
+    test with IEEE division, in the CTA-per-row form (8 rows) and the warp
+    form (7300 rows, more than 48 per SM): codes and scales bit-exact."""
+    X = scaled_rows(M, K, [0, -100, -101, -110, -126, 20], seed=K + M)
+    check_rows(X, cuda_device)
+
+
 def test_empty_rows_call(cuda_device):
     """M = 0 is a no-op (nothing launched) for the quantiser."""
     X = torch.empty((0, 64), dtype=torch.bfloat16, device=cuda_device)
