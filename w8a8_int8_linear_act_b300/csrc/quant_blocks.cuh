@@ -27,6 +27,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "quant_rows.cuh"
 
@@ -92,33 +93,34 @@ __global__ void __launch_bounds__(NV >= 8 ? 256 : 512, NV >= 16 ? 2 : (NV >= 8 ?
     if constexpr (NV > 0) {
         extern __shared__ uint4 s_slots[];
         const int T = static_cast<int>(blockDim.x);
-        auto copy_block = [&](int64_t first, int ntok) {
+        // Blocks of exactly NV passes of every thread (the common case: whole
+        // blocks, every thread active) skip the per-vector range checks.
+        const bool whole_geom = g.tpp * NV == g.block_tokens && g.tpp * g.vd == T;
+        auto copy_block = [&](int64_t first, int ntok, auto whole_c) {
+            constexpr bool kWhole = decltype(whole_c)::value;
 #pragma unroll
             for (int i = 0; i < NV; ++i)
-                if (tok0 + i * g.tpp < ntok) cp_async_16(&s_slots[i * T + t], A + first + i * step);
+                if (kWhole || tok0 + i * g.tpp < ntok) cp_async_16(&s_slots[i * T + t], A + first + i * step);
             cp_async_commit();
         };
-        int64_t blk = blockIdx.x;
-        int ntok = 0;
-        int64_t first = 0;
-        if (blk < nblocks) {
-            first = locate(blk, ntok);
-            copy_block(first, ntok);
-        }
-        for (int it = 0; blk < nblocks; blk += gridDim.x, ++it) {
+        // One block: its vectors from the slots, the absmax, the next block's
+        // copies (once every slot has been read), the scale, the codes.
+        auto run_block = [&](int64_t blk, int it, int64_t first, int ntok, int64_t next_first, int next_ntok,
+                             auto whole_c) {
+            constexpr bool kWhole = decltype(whole_c)::value;
             cp_async_wait_all();
             uint4 v[NV];
 #pragma unroll
-            for (int i = 0; i < NV; ++i) v[i] = tok0 + i * g.tpp < ntok ? s_slots[i * T + t] : make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < NV; ++i)
+                v[i] = (kWhole || tok0 + i * g.tpp < ntok) ? s_slots[i * T + t] : make_uint4(0, 0, 0, 0);
             uint32_t m2 = 0;
 #pragma unroll
             for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
-            // Every v[i] has been read: the slots may take the next block.
-            int next_ntok = 0;
-            int64_t next_first = 0;
-            if (blk + gridDim.x < nblocks) {
-                next_first = locate(blk + gridDim.x, next_ntok);
-                copy_block(next_first, next_ntok);
+            if (next_first >= 0) {
+                if (whole_geom && next_ntok == g.block_tokens)
+                    copy_block(next_first, next_ntok, std::true_type{});
+                else
+                    copy_block(next_first, next_ntok, std::false_type{});
             }
             const RowScale rs = row_scale(block_max(IV::absmax_value(m2), red[it & 1]));
             if (t == 0) S[blk] = rs.s;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(NV >= 8 ? 256 : 512, NV >= 16 ? 2 : (NV >= 8 ?
                 if (rs.corr) {
 #pragma unroll
                     for (int i = 0; i < NV; ++i)
-                        if (tok0 + i * g.tpp < ntok) quantize_vector_corr<false>(v[i], rs, Q, first + i * step);
+                        if (kWhole || tok0 + i * g.tpp < ntok) quantize_vector_corr<false>(v[i], rs, Q, first + i * step);
                 } else if (tok0 < ntok) {
                     quantize_strided_by_tie_test<TIn, false>(A, first, step, (ntok - tok0 + g.tpp - 1) / g.tpp, rs,
                                                              Q);
@@ -134,8 +136,27 @@ __global__ void __launch_bounds__(NV >= 8 ? 256 : 512, NV >= 16 ? 2 : (NV >= 8 ?
             } else {
 #pragma unroll
                 for (int i = 0; i < NV; ++i)
-                    if (tok0 + i * g.tpp < ntok) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
+                    if (kWhole || tok0 + i * g.tpp < ntok) quantize_vector<TIn, false>(v[i], rs, Q, first + i * step);
             }
+        };
+        int64_t blk = blockIdx.x;
+        int ntok = 0;
+        int64_t first = 0;
+        if (blk < nblocks) {
+            first = locate(blk, ntok);
+            if (whole_geom && ntok == g.block_tokens)
+                copy_block(first, ntok, std::true_type{});
+            else
+                copy_block(first, ntok, std::false_type{});
+        }
+        for (int it = 0; blk < nblocks; blk += gridDim.x, ++it) {
+            int next_ntok = 0;
+            int64_t next_first = -1;
+            if (blk + gridDim.x < nblocks) next_first = locate(blk + gridDim.x, next_ntok);
+            if (whole_geom && ntok == g.block_tokens)
+                run_block(blk, it, first, ntok, next_first, next_ntok, std::true_type{});
+            else
+                run_block(blk, it, first, ntok, next_first, next_ntok, std::false_type{});
             first = next_first;
             ntok = next_ntok;
         }

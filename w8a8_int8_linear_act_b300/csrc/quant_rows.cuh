@@ -189,9 +189,10 @@ __device__ __forceinline__ float block_max(float v, float* red /* >= 32 floats *
     if (nwarps == 1) return v;
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    float m = 0.0f;
-    for (int w = 0; w < nwarps; ++w) m = fmaxf(m, red[w]);
-    return m;
+    // Every warp folds the per-warp maxima with shuffles (max is exact and
+    // order-free, so every thread gets the same value).
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    return warp_max(lane < nwarps ? red[lane] : 0.0f);
 }
 
 // round_half_even(clamp(fp32(x / s), -127, 127)) by IEEE division.  Out of
