@@ -85,7 +85,8 @@ typedef enum {
 #define W8A8_REASON_BIAS_DTYPE 0x20  /* bias dtype is not F32 or BF16 */
 
 /* Bits of the device status word (w8a8_read_status). */
-#define W8A8_DEV_TIMEOUT_PRODUCER 0x1  /* TMA producer waited too long for a free stage */
+#define W8A8_DEV_TIMEOUT_PRODUCER 0x1  /* TMA producer waited too long for a free stage (or, in
+                                          w8a8_linear's in-GEMM quantisation, for a tile's rows) */
 #define W8A8_DEV_TIMEOUT_MMA      0x2  /* MMA issuer waited too long for data or accumulator space */
 #define W8A8_DEV_TIMEOUT_EPILOGUE 0x4  /* epilogue waited too long for a finished accumulator */
 #define W8A8_DEV_TIMEOUT_TEARDOWN 0x8  /* in-flight copies or MMAs did not finish at exit */
@@ -195,7 +196,11 @@ W8A8_API int w8a8_gemm_form(int64_t M, int64_t N, int64_t K, int64_t* form);
 /* ---------------------------------------------------------------------------
  * The guarded W8A8 linear: Y = dequant(quant(X) * Wq^T) + bias, in two
  * kernels on `stream`: (1) per-row activation quantisation into the
- * workspace, (2) the tcgen05 GEMM with the fused epilogue.
+ * workspace, (2) the tcgen05 GEMM with the fused epilogue.  For bf16 X with
+ * K = 4096 on the CTA-pair form, (1) quantises only the rows the GEMM's
+ * first wave of tiles reads, and two extra warps of every GEMM CTA quantise
+ * the rest while it runs (each tile waits on the device until its rows are
+ * published); codes, scales and Y are the same bytes either way.
  *   X    [M][K] of `x_dtype` (F32 or BF16)               in
  *   Wp   [N][K] packed weight codes (w8a8_pack_weight)   in
  *   sw   [N]    fp32 weight scales                       in
@@ -218,8 +223,9 @@ W8A8_API w8a8_status w8a8_linear(const void* X, int x_dtype, int64_t M, int64_t 
                         uint16_t* Y, void* ws, size_t ws_bytes, void* stream);
 
 /* The two halves of w8a8_linear, exposed so that each can be timed or
- * reused alone.  w8a8_linear(...) == quant_stage(...) then gemm_stage(...)
- * with the same workspace. */
+ * reused alone.  quant_stage(...) then gemm_stage(...) with the same
+ * workspace gives w8a8_linear's results (the same bytes; w8a8_linear may
+ * overlap the two, as described above). */
 W8A8_API w8a8_status w8a8_linear_quant_stage(const void* X, int x_dtype, int64_t M, int64_t K,
                                     void* ws, size_t ws_bytes, void* stream);
 W8A8_API w8a8_status w8a8_linear_gemm_stage(int64_t M, int64_t K, const uint16_t* Wp, const float* sw,

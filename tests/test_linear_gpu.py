@@ -133,6 +133,68 @@ def test_linear_stages_equal_fused_call(cuda_device):
     assert w8.read_status(ws) == (0, 0)
 
 
+@pytest.mark.parametrize("M,N", [(1600, 4096), (3000, 4096), (6150, 1024), (9000, 2048)])
+def test_linear_in_gemm_quantisation_equals_two_stages(cuda_device, M, N):
+    """With bf16 X and K = 4096, linear() quantises only the rows of the
+    GEMM's first wave up front and the rest inside the GEMM while it runs
+    (ragged last tiles, rows past the first wave in one or several tile
+    groups).  Y, the codes and the row scales are the same bytes as the two
+    stages give, and Y matches the oracle on sampled row blocks."""
+    K = 4096
+    X, W, b = wl.make("video", M=M, N=N, K=K)
+    Xd, bd = X.to(cuda_device), b.to(cuda_device)
+    Wq, sw = w8.quantize_weight(W.to(cuda_device))
+    Wp = w8.pack_weight(Wq)
+    ws1 = torch.empty(w8.workspace_bytes(M, N, K), dtype=torch.uint8, device=cuda_device)
+    ws2 = torch.empty_like(ws1)
+    ws1.fill_(0x5A)   # stale contents must not matter
+    Y1 = w8.linear(Xd, Wp, sw, bd, workspace=ws1)
+    Y2 = torch.empty_like(Y1)
+    w8.linear_quant_stage(Xd, ws2)
+    w8.linear_gemm_stage(M, K, Wp, sw, bd, Y2, ws2)
+    torch.cuda.synchronize()
+    assert w8.read_status(ws1) == (0, 0)
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    # the row scales and the codes in the workspace (layout: 1 KB header,
+    # then sx, then the codes from the next 1 KB boundary)
+    codes_off = 1024 + ((M * 4 + 1023) // 1024) * 1024
+    assert torch.equal(ws1[1024:1024 + M * 4], ws2[1024:1024 + M * 4])
+    assert torch.equal(ws1[codes_off:codes_off + M * K * 2], ws2[codes_off:codes_off + M * K * 2])
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(1500, 1600), np.arange(M - 64, M),
+                                     np.random.default_rng(M).choice(M, 64, replace=False)]))
+    compare(X, W, b, cuda_device, rows=rows[rows < M], what="in-GEMM quantisation")
+
+
+def test_linear_in_gemm_quantisation_timeout_reported(cuda_device):
+    """The in-GEMM quantisation path with the producer issuing no copies (test
+    hook): the rows are still quantised and published, the MMA issuer's and
+    the epilogue's bounded waits run out, the status says so, and the next
+    call is clean and equal to the two-stage result."""
+    M, N, K = 3000, 1024, 4096
+    X, W, b = wl.make("video", M=M, N=N, K=K)
+    Xd, bd = X.to(cuda_device), b.to(cuda_device)
+    Wq, sw = w8.quantize_weight(W.to(cuda_device))
+    Wp = w8.pack_weight(Wq)
+    ws = torch.empty(w8.workspace_bytes(M, N, K), dtype=torch.uint8, device=cuda_device)
+    w8.set_wait_limit_ns(20_000_000)
+    w8.debug_skip_loads(True)
+    try:
+        w8.linear(Xd, Wp, sw, bd, workspace=ws)
+        st, bits_ = w8.read_status(ws)
+    finally:
+        w8.debug_skip_loads(False)
+        w8.set_wait_limit_ns(2_000_000_000)
+    assert st == 7 and bits_ & 0x2 and bits_ & 0x4
+    again = w8.linear(Xd, Wp, sw, bd, workspace=ws)
+    assert w8.read_status(ws) == (0, 0)
+    ws2 = torch.empty_like(ws)
+    Y2 = torch.empty_like(again)
+    w8.linear_quant_stage(Xd, ws2)
+    w8.linear_gemm_stage(M, K, Wp, sw, bd, Y2, ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), Y2.view(torch.int16))
+
+
 def test_linear_output_guard_band(cuda_device):
     """Ragged M/N tiles write nothing outside Y: Y sits inside a larger buffer
     filled with a canary pattern that must survive."""

@@ -67,6 +67,7 @@
 #include <cuda_bf16.h>
 
 #include "ptx_sm103.cuh"
+#include "quant_rows.cuh"
 
 namespace w8a8 {
 
@@ -114,10 +115,25 @@ static_assert(GemmCfg<1>::kStages * GemmCfg<1>::kStageBytes >= kPartialInt4 * 16
 //              tensor memory chunks added in fp32), Y = bf16(acc + b)
 //   kModeW8A8RowMax  kModeW8A8, and each row's max |Y| gathered into
 //              p.row_amax (the next layer's activation scale, MLP pair)
+//   kModeW8A8Fused  kModeW8A8 whose own extra warps quantise the activation
+//              rows [p.q_row0, M) while the GEMM runs (the rows below q_row0
+//              come from the quantiser launched before it); the producers
+//              wait for their rows (K = 4096, bf16 X, CTA pairs)
 constexpr int kModeW8A8 = 0;
 constexpr int kModeS32 = 1;
 constexpr int kModeBf16 = 2;
 constexpr int kModeW8A8RowMax = 3;
+constexpr int kModeW8A8Fused = 4;
+
+// Threads of a GEMM CTA: producer, MMA issuer and the epilogue warps, and in
+// kModeW8A8Fused two quantiser warps (12 warps x 32 x 168 registers still
+// fit the register file, three warps per sub-partition).
+constexpr int kFusedQuantWarps = 2;
+__host__ __device__ constexpr int gemm_threads(int mode)
+{
+    return kGemmThreads + (mode == kModeW8A8Fused ? 32 * kFusedQuantWarps : 0);
+}
+constexpr int kFusedQuantK = 4096;   // row length the quantiser warps take (16 vectors a lane)
 
 // Status bits (same values as W8A8_DEV_* in the public header).
 constexpr uint32_t kDevTimeoutProducer = 0x1;
@@ -143,6 +159,15 @@ struct GemmParams {
     uint32_t* row_amax;        // [M] (kModeW8A8RowMax): each row's max |Y| as fp32 bits, by atomicMax
     uint64_t wait_limit_ns;
     int32_t skip_loads;        // test hook: producer issues no copies
+    // kModeW8A8Fused: the bf16 activation, its code and scale buffers (the
+    // ones the A tensor map and sx point at), the first row the quantiser
+    // warps take (a multiple of 256), and per 256-row tile the number of its
+    // rows finished.  status[1] counts rows claimed from q_row0 on.
+    const __nv_bfloat16* qx;
+    uint16_t* qcodes;
+    float* qsx;
+    int32_t q_row0;
+    uint32_t* q_ready;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int& mb, int& nb)
@@ -184,13 +209,68 @@ __device__ __forceinline__ bool worker_unit(const GemmParams& p, int num_kb, int
     return false;
 }
 
+// kModeW8A8Fused: one quantiser warp.  Rows q_row0 + 0, 1, ... are claimed
+// in order (status[1]); a row is held in registers (16 vectors a lane),
+// reduced, coded by the row rule of quant_rows.cuh and its scale written,
+// then counted into its 256-row tile's q_ready word (a fence, then the
+// add: release).  The next claim is taken while the current row is worked
+// on.  Any resident CTA makes progress on any row, and no quantiser warp
+// waits on another, so the producers that wait for a tile's rows never wait
+// on a CTA that is not running.
+__device__ __forceinline__ void fused_quant_warp(const GemmParams& p)
+{
+    constexpr int NV = kFusedQuantK / 8 / 32;
+    using IV = InVec<__nv_bfloat16>;
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    uint32_t* claimed = p.status + 1;
+    uint32_t claim = 0;
+    if (lane == 0) claim = atomicAdd(claimed, 1u);
+    claim = __shfl_sync(0xFFFFFFFFu, claim, 0);
+    while (static_cast<int64_t>(p.q_row0) + claim < p.M) {
+        const int64_t row = static_cast<int64_t>(p.q_row0) + claim;
+        uint32_t next = 0;
+        if (lane == 0) next = atomicAdd(claimed, 1u);
+        const uint4* src = reinterpret_cast<const uint4*>(p.qx + row * kFusedQuantK);
+        uint4 v[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = load_stream(src + lane + 32 * i);
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) IV::absmax(v[i], m2);
+        const RowScale rs = row_scale(warp_max(IV::absmax_value(m2)));
+        if (lane == 0) p.qsx[row] = rs.s;
+        const int64_t out0 = row * kFusedQuantK;
+        if (rs.corr) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                quantize_vector_corr<true>(v[i], rs, p.qcodes, out0 + static_cast<int64_t>(lane + 32 * i) * 8);
+        } else {
+            quantize_strided_by_tie_test<__nv_bfloat16, true>(p.qx, out0 + lane * 8, 32 * 8, NV, rs, p.qcodes);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();   // this row's codes and scale before its count
+            atomicAdd(p.q_ready + (row >> 8), 1u);
+        }
+        claim = __shfl_sync(0xFFFFFFFFu, next, 0);
+    }
+}
+
+// kModeW8A8Fused: waits until the 256-row tile `t` (t * 256 >= q_row0) has
+// all its rows, with acquire semantics.
+__device__ __forceinline__ bool fused_tile_ready(const GemmParams& p, int t, uint64_t limit)
+{
+    const uint32_t rows = static_cast<uint32_t>(min(256, p.M - t * 256));
+    return wait_counter_ge(p.q_ready + t, rows, limit);
+}
+
 __device__ __forceinline__ void epi_barrier()
 {
     asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(32 * kEpiWarps) : "memory");
 }
 
 template <int kMode, int kPair>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(kMode), 1)
     gemm_w8a8_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                              const __grid_constant__ CUtensorMap tmap_y, const GemmParams p)
 {
@@ -231,7 +311,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr bool kOutS32 = kMode == kModeS32;
     constexpr bool kFp32Sums = kMode == kModeBf16;   // sums held as fp32 bit patterns (zero bits = +0.0f)
     constexpr bool kRowMax = kMode == kModeW8A8RowMax;
-    constexpr bool kScaled = kMode == kModeW8A8 || kRowMax;   // INT8 codes dequantised by sx and sw
+    constexpr bool kFusedQuant = kMode == kModeW8A8Fused;
+    constexpr bool kScaled = kMode == kModeW8A8 || kRowMax || kFusedQuant;   // INT8 codes dequantised by sx and sw
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -281,6 +362,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tile_coords(u.tile, tiles_m, tiles_n, p.group_m, mb, nb);
                 const int a_row = (mb * kPair + static_cast<int>(rank)) * kBM;
                 const int b_row = nb * kBN + static_cast<int>(rank) * C::kBRows;
+                if constexpr (kFusedQuant) {
+                    // The tile's rows must be quantised first.
+                    const int t256 = (mb * kPair * kBM) >> 8;
+                    if (t256 * 256 >= p.q_row0) {
+                        if (!fused_tile_ready(p, t256, limit)) {
+                            atomicOr(p.status, kDevTimeoutProducer);
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_global();   // the copies below read what generic stores wrote
+                    }
+                }
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S);
                     const uint32_t ph = (it / S) & 1u;
@@ -386,6 +479,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mma_commit<kPair>(done, 0x1);
             if (!mbar_wait(done, 0, limit)) atomicOr(p.status, kDevTimeoutTeardown);
         }
+    } else if (kFusedQuant && warp >= 2 + kEpiWarps) {
+        // ------------------------------------------------------------ activation rows
+        fused_quant_warp(p);
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;        // TMEM lanes this warp may read
@@ -413,6 +509,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     s_bias[i] = n < p.N ? __uint_as_float(static_cast<uint32_t>(
                                               static_cast<const uint16_t*>(p.bias)[n]) << 16)
                                         : 0.0f;
+                if constexpr (kFusedQuant) {
+                    // The row's scale once the tile's rows are published (the
+                    // producer waits for the same rows before the first copy,
+                    // so this wait ends before the first chunk is ready).
+                    if (m < p.M && m >= p.q_row0 && !fused_tile_ready(p, m >> 8, limit))
+                        atomicOr(p.status, kDevTimeoutEpilogue);
+                }
                 if (kScaled && m < p.M) sxm = p.sx[m];
             }
             int32_t acc[128];

@@ -192,6 +192,32 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
 }
 
+// A 32-bit counter in global memory shared by the CTAs of one grid: an
+// acquire load, a release store, and a bounded wait until it reaches a
+// value (false when limit_ns ran out first).
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u32(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool wait_counter_ge(const uint32_t* p, uint32_t target, uint64_t limit_ns)
+{
+    if (ld_acquire_gpu_u32(p) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire_gpu_u32(p) >= target) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 {
     uint32_t done;

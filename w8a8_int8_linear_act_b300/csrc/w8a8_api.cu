@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -418,7 +419,8 @@ bool ensure_gemm_ready(DeviceInfo* dev)
     if (set_gemm_smem<kModeW8A8, 1>() != cudaSuccess || set_gemm_smem<kModeS32, 1>() != cudaSuccess ||
         set_gemm_smem<kModeBf16, 1>() != cudaSuccess || set_gemm_smem<kModeW8A8, 2>() != cudaSuccess ||
         set_gemm_smem<kModeS32, 2>() != cudaSuccess || set_gemm_smem<kModeBf16, 2>() != cudaSuccess ||
-        set_gemm_smem<kModeW8A8RowMax, 1>() != cudaSuccess || set_gemm_smem<kModeW8A8RowMax, 2>() != cudaSuccess) {
+        set_gemm_smem<kModeW8A8RowMax, 1>() != cudaSuccess || set_gemm_smem<kModeW8A8RowMax, 2>() != cudaSuccess ||
+        set_gemm_smem<kModeW8A8Fused, 1>() != cudaSuccess || set_gemm_smem<kModeW8A8Fused, 2>() != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -653,14 +655,57 @@ w8a8_status launch_kcluster(const KcPlan& kp, const uint16_t* A_codes, const uin
     return last_launch_status();
 }
 
+// The W8A8 linear with its activation quantisation overlapped with the GEMM
+// (kModeW8A8Fused): for bf16 X with K = 4096 on the CTA-pair form, when the
+// GEMM's first wave of tiles needs fewer rows than there are.  Where the
+// weights fit well in L2, the tiles are rasterised in groups of 2 row-tiles
+// instead of 8, so that the first wave touches few row-tiles (larger weights
+// keep groups of 8: re-reading them from HBM every 2 row-tiles cost more than
+// the overlap gains).  The first wave's rows (the head) are quantised before
+// the GEMM by the row quantiser, the rest by the GEMM's own quantiser warps
+// while it runs.  Returns the head's row count, or 0 where the fused form
+// does not apply.
+int fused_group_m(int64_t N, int64_t K) { return N * K * 2 <= (int64_t(64) << 20) ? 2 : 8; }
+
+int64_t fused_head_rows(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, int x_dtype, int64_t slots)
+{
+    if (x_dtype != W8A8_BF16 || K != w8a8::kFusedQuantK || g_force_form.load() >= 0) return 0;
+    const GemmPlan g = choose_plan(M, N, K, dev->num_sms, dev->pair_workers, slots);
+    if (g.pair != 2) return 0;
+    const int tiles_m = static_cast<int>((M + 2 * w8a8::kBM - 1) / (2 * w8a8::kBM));
+    const int tiles_n = static_cast<int>((N + w8a8::kBN - 1) / w8a8::kBN);
+    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    const int workers = g.grid / 2;
+    // Row-tiles of the first wave: the whole tiles its workers start with,
+    // and, where the wave reaches the split tail, every tail tile.
+    int max_mb = 0;
+    const int64_t first = std::min<int64_t>(workers, g.dp_tiles);
+    const int group_m = fused_group_m(N, K);
+    for (int64_t t = 0; t < first; ++t) {
+        const int per_group = group_m * tiles_n;
+        const int gi = static_cast<int>(t / per_group);
+        const int first_m = gi * group_m;
+        const int gsz = std::min(tiles_m - first_m, group_m);
+        const int r = static_cast<int>(t - static_cast<int64_t>(gi) * per_group);
+        max_mb = std::max(max_mb, first_m + r % gsz);
+    }
+    if (workers > g.dp_tiles) max_mb = tiles_m - 1;   // the wave reaches the tail tiles
+    const int64_t head = std::min<int64_t>(M, static_cast<int64_t>(max_mb + 1) * 2 * w8a8::kBM);
+    // The per-tile row counts sit at the top of the header, above the split
+    // tiles' counters.
+    const int64_t split_counters = (tiles - g.dp_tiles) * 2;
+    if (static_cast<int64_t>(kCounterOffWords) + split_counters + tiles_m > w8a8::kHeaderWords) return 0;
+    return head < M ? head : 0;
+}
+
 template <int kMode>
 w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t* Wp, int64_t M, int64_t N,
                         int64_t K, const float* sx, const float* sw, const void* bias, int bias_mode, void* out,
                         uint8_t* ws_aligned, const WsLayout& L, int64_t slots, cudaStream_t stream,
-                        uint32_t* row_amax = nullptr)
+                        uint32_t* row_amax = nullptr, const uint16_t* fused_x = nullptr, int64_t fused_row0 = 0)
 {
     if (!ensure_gemm_ready(dev)) return W8A8_ERR_CUDA;
-    if constexpr (kMode != w8a8::kModeW8A8RowMax) {
+    if constexpr (kMode != w8a8::kModeW8A8RowMax && kMode != w8a8::kModeW8A8Fused) {
         // Few output tiles: the cluster-K form spreads them over the SMs.
         const KcPlan kp = current_kc_plan(dev, M, N, K);
         if (kp.bn != 0)
@@ -685,7 +730,7 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     // fp32 accumulation over the unit's whole K range.
     p.kb_per_chunk = kMode == w8a8::kModeBf16 ? static_cast<int32_t>((K + w8a8::kBK - 1) / w8a8::kBK)
                                               : w8a8::kMaxKbPerChunk;
-    p.group_m = 8;
+    p.group_m = kMode == w8a8::kModeW8A8Fused ? fused_group_m(N, K) : 8;
     p.bias_mode = bias_mode;
     p.sx = sx;
     p.sw = sw;
@@ -701,6 +746,11 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     p.splits = g.splits;
     p.tail_units = static_cast<int32_t>(g.tail_units);
     p.row_amax = row_amax;
+    p.qx = reinterpret_cast<const __nv_bfloat16*>(fused_x);
+    p.qcodes = const_cast<uint16_t*>(A_codes);
+    p.qsx = const_cast<float*>(sx);
+    p.q_row0 = static_cast<int32_t>(fused_row0);
+    p.q_ready = header + (w8a8::kHeaderWords - (M + 255) / 256);   // per 256-row tile, in the zeroed header
     // A programmatic dependent of the kernel before it in the stream (the
     // quantiser that writes its codes): its set-up overlaps that kernel's
     // tail, and it waits on the device for its results (griddepcontrol).
@@ -713,7 +763,7 @@ w8a8_status launch_gemm(DeviceInfo* dev, const uint16_t* A_codes, const uint16_t
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(g.grid));
-    cfg.blockDim = dim3(w8a8::kGemmThreads);
+    cfg.blockDim = dim3(w8a8::gemm_threads(kMode));
     cfg.stream = stream;
     cfg.attrs = attr;
     cudaError_t err;
@@ -1127,6 +1177,28 @@ w8a8_status w8a8_linear(const void* X, int x_dtype, int64_t M, int64_t K, const 
     if (!aligned(X, 16) || !aligned(Wp, 16) || !aligned(Y, 16) || !aligned(ws, 16) || !aligned(sw, 16))
         return W8A8_ERR_ALIGNMENT;
     if (bias && !aligned(bias, 16)) return W8A8_ERR_ALIGNMENT;
+    if (M > 0 && N > 0 && K > 0) {
+        int devno = 0;
+        DeviceInfo* dev = const_cast<DeviceInfo*>(device_info(&devno));
+        if (!dev) return W8A8_ERR_NO_DEVICE;
+        if (!ensure_gemm_ready(dev)) return W8A8_ERR_CUDA;
+        const int64_t head = fused_head_rows(dev, M, N, K, x_dtype, ws_slots(L, ws_bytes));
+        if (head > 0) {
+            // The head rows now (the launch also clears the workspace header,
+            // which holds the row counters), the rest inside the GEMM.
+            uint8_t* w = ws_base(ws);
+            cudaStream_t s = static_cast<cudaStream_t>(stream);
+            w8a8_status st = launch_quant<true>(X, x_dtype, head, K, w + L.codes_off,
+                                                reinterpret_cast<float*>(w + L.sx_off),
+                                                reinterpret_cast<uint32_t*>(w + L.status_off), s);
+            if (st != W8A8_OK) return st;
+            const int bias_mode = bias ? (bias_dtype == W8A8_F32 ? 1 : 2) : 0;
+            return launch_gemm<w8a8::kModeW8A8Fused>(
+                dev, reinterpret_cast<const uint16_t*>(w + L.codes_off), Wp, M, N, K,
+                reinterpret_cast<const float*>(w + L.sx_off), sw, bias, bias_mode, Y, w, L, ws_slots(L, ws_bytes), s,
+                nullptr, static_cast<const uint16_t*>(X), head);
+        }
+    }
     w8a8_status st = w8a8_linear_quant_stage(X, x_dtype, M, K, ws, ws_bytes, stream);
     if (st != W8A8_OK) return st;
     return w8a8_linear_gemm_stage(M, K, Wp, sw, N, bias, bias_dtype, Y, ws, ws_bytes, stream);
