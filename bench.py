@@ -55,7 +55,7 @@ PER_WORKLOAD_COLD = 50        # cold-L2 steps per per-workload measurement
 PER_WORKLOAD_GRAPH = 50       # steps per captured graph (hot L2)
 PER_WORKLOAD_REPLAYS = 5      # graph replays per hot-L2 measurement
 
-# Algorithmic bytes (the method's, SURVEY-style accounting with INT8 codes):
+# Algorithmic bytes (the method's own accounting, with INT8 codes of 1 B):
 #   quantiser per activation element: input (2 B bf16, 4 B fp32) + 1 B int8 code; + 4 B per row (scale)
 #   GEMM per launch: Xq (M K) + Wq (N K) + sx (4 M) + sw (4 N) + bias (2 N or 4 N) + Y (2 M N)
 # Bytes as built (the codes are carried as bf16 for the tensor cores):
