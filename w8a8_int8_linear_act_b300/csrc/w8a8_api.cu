@@ -661,14 +661,14 @@ w8a8_status launch_kcluster(const KcPlan& kp, const uint16_t* A_codes, const uin
 // The W8A8 linear with its activation quantisation overlapped with the GEMM
 // (kModeW8A8Fused): for bf16 X with K = 4096 on the CTA-pair form, when the
 // GEMM's first wave of tiles needs fewer rows than there are.  Where the
-// weights fit well in L2, the tiles are rasterised in groups of 2 row-tiles
-// instead of 8, so that the first wave touches few row-tiles (larger weights
-// keep groups of 8: re-reading them from HBM every 2 row-tiles cost more than
-// the overlap gains).  The first wave's rows (the head) are quantised before
+// weights fit well in L2, the tiles are rasterised row-tile by row-tile
+// instead of in groups of 8, so that the first wave touches few row-tiles
+// (larger weights keep groups of 8: re-reading them from HBM every few
+// row-tiles cost more than the overlap gains).  The first wave's rows (the head) are quantised before
 // the GEMM by the row quantiser, the rest by the GEMM's own quantiser warps
 // while it runs.  Returns the head's row count, or 0 where the fused form
 // does not apply.
-int fused_group_m(int64_t N, int64_t K) { return N * K * 2 <= (int64_t(64) << 20) ? 2 : 8; }
+int fused_group_m(int64_t N, int64_t K) { return N * K * 2 <= (int64_t(64) << 20) ? 1 : 8; }
 
 int64_t fused_head_rows(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, int x_dtype, int64_t slots)
 {
