@@ -22,11 +22,13 @@
 // for K <= 4096; a CTA per row up to 32768), with the row held in registers
 // through three reductions: the sum (LayerNorm), the sum of squared
 // deviations, and the absmax of y.  The warp form is persistent: CTAs of
-// eight warps, as many as fit on the GPU at once, each preparing the
-// modulation once in shared memory as fp32 (1 + scale, shift); each warp
-// works through rows grid-stride, and copies its next row into a buffer of
-// its own in shared memory while the current row's arithmetic runs, so that
-// HBM keeps streaming during the arithmetic.  The per-element arithmetic
+// eight or sixteen warps, as many as fit on the GPU at once (at most one per
+// row), each preparing the modulation once in shared memory as fp32
+// (1 + scale, shift); the rows are dealt to the CTAs in turn, so that every
+// SM gets rows even when there are few, and each warp works through its
+// rows grid-stride, copying its next row into a buffer of its own in shared
+// memory while the current row's arithmetic runs, so that HBM keeps
+// streaming during the arithmetic.  The per-element arithmetic
 // runs on packed pairs of fp32 (f32x2), one instruction for two elements.
 #pragma once
 
@@ -285,16 +287,17 @@ __device__ __forceinline__ void norm_quant_row(const __nv_bfloat16* __restrict__
 }
 
 // kRowsPerCta > 1 (warp form): a CTA of kRowsPerCta warps stages the
-// modulation once, then each warp takes rows warp, warp + stride, ... of the
-// whole grid (stride = gridDim.x * kRowsPerCta); the launcher sizes the
-// grid to the CTAs that fit on the GPU at once, so that every warp works
+// modulation once, then warp w of CTA c takes rows w * gridDim.x + c,
+// + stride, ... (stride = gridDim.x * kRowsPerCta: consecutive rows go to
+// consecutive CTAs); the launcher sizes the grid to the CTAs that fit on
+// the GPU at once (and at most one per row), so that every warp works
 // through several rows, its next row streaming into its shared-memory
 // buffer while it computes on the current one.  Dynamic shared memory:
 // the modulation (8 B per element of a row), then a row buffer per warp
 // (2 B per element).  kRowsPerCta == 1: a CTA per row (long rows).
 // kFull (warp form only): K = 256 NV.
 template <bool kBf16Codes, int NV, int kRowsPerCta, bool kFull, int kNorm>
-__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRowsPerCta > 1 ? 2 : 1)
+__global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRowsPerCta > 1 && kRowsPerCta < 16 ? 2 : 1)
     norm_quant_rows_kernel(const __nv_bfloat16* __restrict__ A, int64_t R, int64_t K, NormParams np,
                            void* __restrict__ Q, float* __restrict__ S, uint32_t* __restrict__ header)
 {
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kRowsPerCta > 1 ? 32 * kRowsPerCta : 256, kRow
         }
         const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowsPerCta;
         const int lane = static_cast<int>(threadIdx.x & 31);
-        int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+        int64_t row = static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x;
         uint4* buf = reinterpret_cast<uint4*>(s_mod + 4 * V) + (threadIdx.x >> 5) * V;
         if (row < R) copy_row_async<NV, kFull>(A, row, K, buf, lane);
         __syncthreads();

@@ -874,10 +874,12 @@ template <bool kBf16Codes, int NV, int kRows, bool kFull, int kNorm>
 void launch_norm_cfg(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormParams& np, void* Q, float* S,
                      uint32_t* header, unsigned threads, cudaStream_t stream)
 {
-    int64_t blocks = (M + kRows - 1) / kRows;
-    // The warp form stages the fp32 modulation in shared memory, 8 B per
-    // element of a row, and a row buffer per warp, 2 B per element (96 KB at
-    // the largest, K = 4096, eight warps).
+    // A CTA per row; the warp form (rows dealt to the CTAs in turn) caps that
+    // at the CTAs that fit at once below.  The warp form stages the fp32
+    // modulation in shared memory, 8 B per element of a row, and a row buffer
+    // per warp, 2 B per element (160 KB at the largest, K = 4096, sixteen
+    // warps).
+    int64_t blocks = M;
     const size_t smem = kRows > 1 ? static_cast<size_t>(K) * (8u + 2u * kRows) : 0u;
     if constexpr (kRows > 1) {
         // Persistent warps: no more CTAs than fit on the GPU at once.
@@ -904,10 +906,13 @@ void launch_norm_cfg(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormPa
                                                                    np, Q, S, header);
 }
 
-// Rows of up to 128 vectors: a warp per row with 4 vectors per lane; up to
-// 512: 16 per lane; up to 4096 (K <= 32768): a CTA per row, 16 per thread.
-// Rows of exactly 128, 256 or 512 vectors (K = 1024, 2048, 4096) take the
-// warp form with 4, 8 or 16 vectors per lane and no range checks.
+// Rows of up to 128 vectors: a warp per row with 4 vectors per lane, CTAs
+// of eight warps; up to 512: 16 per lane, CTAs of sixteen warps (one per
+// SM); up to 4096 (K <= 32768): a CTA per row, 16 per thread.  Rows of
+// exactly 128, 256 or 512 vectors (K = 1024, 2048, 4096) take the warp form
+// with 4, 8 or 16 vectors per lane and no range checks.  Sixteen-warp CTAs
+// at K = 4096 measured 10 % faster than two CTAs of eight per SM at 6144
+// rows (one CTA then stages the modulation for sixteen warps).
 template <bool kBf16Codes, int kNorm>
 w8a8_status launch_norm_typed(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormParams& np, void* Q,
                               float* S, uint32_t* header, cudaStream_t stream)
@@ -918,11 +923,11 @@ w8a8_status launch_norm_typed(const uint16_t* X, int64_t M, int64_t K, const w8a
     else if (V == 256)
         launch_norm_cfg<kBf16Codes, 8, 8, true, kNorm>(X, M, K, np, Q, S, header, 256, stream);
     else if (V == 512)
-        launch_norm_cfg<kBf16Codes, 16, 8, true, kNorm>(X, M, K, np, Q, S, header, 256, stream);
+        launch_norm_cfg<kBf16Codes, 16, 16, true, kNorm>(X, M, K, np, Q, S, header, 512, stream);
     else if (V <= 128)
         launch_norm_cfg<kBf16Codes, 4, 8, false, kNorm>(X, M, K, np, Q, S, header, 256, stream);
     else if (V <= 512)
-        launch_norm_cfg<kBf16Codes, 16, 8, false, kNorm>(X, M, K, np, Q, S, header, 256, stream);
+        launch_norm_cfg<kBf16Codes, 16, 16, false, kNorm>(X, M, K, np, Q, S, header, 512, stream);
     else {
         const unsigned T = static_cast<unsigned>(((V + 15) / 16 + 31) / 32 * 32);
         launch_norm_cfg<kBf16Codes, 16, 1, false, kNorm>(X, M, K, np, Q, S, header, T, stream);
