@@ -109,6 +109,10 @@ def mod_vectors(K, seed, dtype):
     (129, 1024, "rms", torch.bfloat16),     # whole rows of 4 vectors per lane
     (77, 2048, "rms", torch.float32),       # whole rows of 8 vectors per lane
     (3001, 1040, "layer", torch.bfloat16),  # more rows than warps on the GPU, ragged lanes
+    (5, 4096, "rms", torch.bfloat16),       # fewer rows than SMs: one CTA per row, one warp busy
+    (126, 4096, "layer", None),             # the audio row count: most CTAs take one row
+    (2500, 4096, "rms", torch.float32),     # just past one round of the sixteen-warp CTAs
+    (2500, 3968, "layer", torch.bfloat16),  # the same with ragged lanes (496 vectors a row)
 ])
 def test_norm_quant_shapes(cuda_device, M, K, kind, mod):
     g = torch.Generator().manual_seed(M + K)
