@@ -664,10 +664,10 @@ w8a8_status launch_kcluster(const KcPlan& kp, const uint16_t* A_codes, const uin
 // weights fit well in L2, the tiles are rasterised row-tile by row-tile
 // instead of in groups of 8, so that the first wave touches few row-tiles
 // (larger weights keep groups of 8: re-reading them from HBM every few
-// row-tiles cost more than the overlap gains).  The first wave's rows (the head) are quantised before
-// the GEMM by the row quantiser, the rest by the GEMM's own quantiser warps
-// while it runs.  Returns the head's row count, or 0 where the fused form
-// does not apply.
+// row-tiles cost more than the overlap gains).  The first wave's rows (the
+// head) are quantised before the GEMM by the row quantiser, the rest by the
+// GEMM's own quantiser warps while it runs.  Returns the head's row count,
+// or 0 where the fused form does not apply.
 int fused_group_m(int64_t N, int64_t K) { return N * K * 2 <= (int64_t(64) << 20) ? 1 : 8; }
 
 int64_t fused_head_rows(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K, int x_dtype, int64_t slots)
@@ -910,9 +910,10 @@ void launch_norm_cfg(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormPa
 // of eight warps; up to 512: 16 per lane, CTAs of sixteen warps (one per
 // SM); up to 4096 (K <= 32768): a CTA per row, 16 per thread.  Rows of
 // exactly 128, 256 or 512 vectors (K = 1024, 2048, 4096) take the warp form
-// with 4, 8 or 16 vectors per lane and no range checks.  Sixteen-warp CTAs
-// at K = 4096 measured 10 % faster than two CTAs of eight per SM at 6144
-// rows (one CTA then stages the modulation for sixteen warps).
+// with 4, 8 or 16 vectors per lane (CTAs of eight, eight and sixteen warps)
+// and no range checks.  Sixteen-warp CTAs at K = 4096 measured 10 % faster
+// than two CTAs of eight per SM at 6144 rows (one CTA then stages the
+// modulation for sixteen warps).
 template <bool kBf16Codes, int kNorm>
 w8a8_status launch_norm_typed(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormParams& np, void* Q,
                               float* S, uint32_t* header, cudaStream_t stream)
