@@ -834,7 +834,9 @@ def run_ours(args):
     # A spin of about 2 ms on the stream, outside every timed interval: the
     # host then enqueues the steps while the GPU is busy, so that no step's
     # interval includes the host's launch latency (the first step's did).
-    torch.cuda._sleep(SPIN_BEFORE_STEPS_CYCLES)
+    spin = getattr(torch.cuda, "_sleep", None)
+    if spin is not None:
+        spin(SPIN_BEFORE_STEPS_CYCLES)
     for i in range(args.steps):
         flush.zero_()
         evs[i][0].record(stream)
