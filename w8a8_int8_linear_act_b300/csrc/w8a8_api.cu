@@ -54,6 +54,20 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per device (the attribute belongs to each device's context).  `done` is
+// the kernel's own per-device flag array.  A failure leaves the flag clear
+// (the launch then fails and reports W8A8_ERR_CUDA).
+void set_dynamic_smem_once(const void* func, int bytes, std::atomic<bool>* done)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices && !done[dev].load()) {
+        if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess)
+            done[dev].store(true);
+    }
+    cudaGetLastError();
+}
+
 // Per-device facts, queried once.  Returns nullptr when the current device
 // cannot run sm_103a code.
 const DeviceInfo* device_info(int* dev_out)
@@ -883,12 +897,10 @@ void launch_norm_cfg(const uint16_t* X, int64_t M, int64_t K, const w8a8::NormPa
     const size_t smem = kRows > 1 ? static_cast<size_t>(K) * (8u + 2u * kRows) : 0u;
     if constexpr (kRows > 1) {
         // Persistent warps: no more CTAs than fit on the GPU at once.
-        static std::once_flag attr_once;
-        std::call_once(attr_once, [] {
-            cudaFuncSetAttribute(w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kFull, kNorm>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 4096 * (8 + 2 * kRows));
-            cudaGetLastError();
-        });
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_dynamic_smem_once(reinterpret_cast<const void*>(
+                                  w8a8::norm_quant_rows_kernel<kBf16Codes, NV, kRows, kFull, kNorm>),
+                              4096 * (8 + 2 * kRows), attr_done);
         const DeviceInfo* dev = device_info(nullptr);
         int per_sm = 0;
         if (dev != nullptr &&
@@ -982,12 +994,9 @@ void launch_blocks_cfg(const TIn* X, const w8a8::BlockGeom& g, int64_t blocks, i
     const size_t smem = NV > 0 ? static_cast<size_t>(NV) * threads * 16u : 0u;
     int64_t grid = blocks;
     if constexpr (NV > 0) {
-        static std::once_flag attr_once;
-        std::call_once(attr_once, [] {
-            cudaFuncSetAttribute(w8a8::quant_blocks_kernel<TIn, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 NV * (NV >= 8 ? kBlockThreads : kBlockThreadsWide) * 16);
-            cudaGetLastError();
-        });
+        static std::atomic<bool> attr_done[kMaxDevices];
+        set_dynamic_smem_once(reinterpret_cast<const void*>(w8a8::quant_blocks_kernel<TIn, NV>),
+                              NV * (NV >= 8 ? kBlockThreads : kBlockThreadsWide) * 16, attr_done);
         const DeviceInfo* dev = device_info(nullptr);
         int per_sm = 0;
         if (dev != nullptr &&
