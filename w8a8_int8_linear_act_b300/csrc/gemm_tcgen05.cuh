@@ -98,10 +98,21 @@ struct GemmCfg {
     static constexpr uint32_t kStagingBytes = kPair == 2 ? kEpiWarps * 4096 : 0;
     static constexpr uint32_t kParamBytes = 2 * kBN * 4;            // the tile's sw and bias, fp32
     static constexpr size_t kSmemBytes =
-        1024 /* alignment slack */ + kStages * kStageBytes + kStagingBytes + kParamBytes + 256 /* barriers */;
+        1024 /* alignment slack */ + kStages * kStageBytes + kStagingBytes + kParamBytes + 512 /* barriers */;
 };
 static_assert(GemmCfg<1>::kSmemBytes <= 227 * 1024 && GemmCfg<2>::kSmemBytes <= 227 * 1024, "shared memory");
-static_assert((2 * GemmCfg<2>::kStages + 7) * 8 + 8 <= 256 && (2 * GemmCfg<1>::kStages + 7) * 8 + 8 <= 256,
+// Split fix-up: each epilogue warp streams its region of the other
+// segments' partial tiles through kFixSlots slots of kFixSlotBytes in the
+// idle operand ring (and output staging), kFixWarpBytes per warp.
+constexpr int kFixSlots = 3;
+constexpr uint32_t kFixSlotBytes = 8192;                        // half of a warp's 16 KB region of a partial
+constexpr uint32_t kFixWarpBytes = kFixSlots * kFixSlotBytes;
+static_assert(kEpiWarps * kFixWarpBytes <= GemmCfg<2>::kStages * GemmCfg<2>::kStageBytes +
+                                               GemmCfg<2>::kStagingBytes &&
+                  kEpiWarps * kFixWarpBytes <= GemmCfg<1>::kStages * GemmCfg<1>::kStageBytes,
+              "fix-up slots fit in the ring and staging");
+static_assert((2 * GemmCfg<2>::kStages + 7 + kEpiWarps * kFixSlots) * 8 <= 512 &&
+                  (2 * GemmCfg<1>::kStages + 7 + kEpiWarps * kFixSlots) * 8 <= 512,
               "barrier area");
 static_assert(GemmCfg<1>::kStages * GemmCfg<1>::kStageBytes >= kPartialInt4 * 16 &&
                   GemmCfg<2>::kStages * GemmCfg<2>::kStageBytes >= kPartialInt4 * 16,
@@ -290,12 +301,12 @@ __global__ void __launch_bounds__(gemm_threads(kMode), 1)
     uint64_t* tfull = bars + 2 * S;           // [2] MMA -> epilogue
     uint64_t* tempty = tfull + 2;             // [2] epilogue -> MMA (the leader's counts both CTAs)
     uint64_t* done = tempty + 2;              // MMA teardown
-    uint64_t* fixbar = done + 1;              // split fix-up: partial tiles copied into the idle ring
-    uint64_t* peerbar = fixbar + 1;           // pair teardown: the peer's count of issued loads has arrived
+    uint64_t* peerbar = done + 1;             // pair teardown: the peer's count of issued loads has arrived
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(peerbar + 1);
     uint32_t* peer_issued = tmem_holder + 1;  // pair teardown: loads the peer's producer issued
+    uint64_t* fixbars = peerbar + 2;          // [kEpiWarps][kFixSlots] split fix-up: a slot's copy landed
     __shared__ int s_last_arrival;
-    __shared__ int s_fix_status;   // split fix-up: 1 partial copied, 2 its copy timed out
+    __shared__ int s_fix_status;   // split fix-up: 0 every copy landed, 1 a copy timed out
     __shared__ int s_chunk_ready[2];
 
     const int warp = threadIdx.x >> 5;
@@ -324,8 +335,8 @@ __global__ void __launch_bounds__(gemm_threads(kMode), 1)
             mbar_init(&tempty[b], kPair * kEpiWarps);
         }
         mbar_init(done, 1);
-        mbar_init(fixbar, 1);
         mbar_init(peerbar, 1);
+        for (int i = 0; i < kEpiWarps * kFixSlots; ++i) mbar_init(&fixbars[i], 1);
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
@@ -567,7 +578,8 @@ __global__ void __launch_bounds__(gemm_threads(kMode), 1)
                 // count in, and only the last segment to arrive finishes this
                 // CTA's rows of the tile.  Thread (e, lane) always holds the
                 // same 128 sums, so the slots use a layout in which each warp
-                // access is 512 contiguous bytes.
+                // access is 512 contiguous bytes, and epilogue warp e's sums
+                // fill the 16 KB region e of the slot.
                 int4* mine = p.partials + (static_cast<int64_t>(u.slot) * kPair + rank) * kPartialInt4;
 #pragma unroll
                 for (int g = 0; g < 32; ++g)
@@ -575,6 +587,10 @@ __global__ void __launch_bounds__(gemm_threads(kMode), 1)
                            make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
                 fence_proxy_async_global();   // the last segment reads the slot by bulk copy
                 __threadfence();
+                // The fix-up below reuses the output staging: the previous
+                // tile's stores must have finished reading it.
+                if (kPair == 2 && !kOutS32 && lane == 0) bulk_wait_read_all();
+                if (e == 0 && lane == 0) s_fix_status = 0;
                 epi_barrier();
                 const int counter = (u.tile - p.dp_tiles) * kPair + static_cast<int>(rank);
                 if (e == 0 && lane == 0)
@@ -583,14 +599,14 @@ __global__ void __launch_bounds__(gemm_threads(kMode), 1)
                 epi_barrier();
                 if (!s_last_arrival) continue;
                 __threadfence();
-                // This was the CTA's last unit, so its operand ring is idle (the
-                // MMAs that read it are complete): each other segment's partial
-                // comes in as one asynchronous bulk copy of 128 KB into the ring
-                // and is added from shared memory, instead of as rounds of
-                // dependent L2 loads.
-                const int first = (u.tile - p.dp_tiles) * p.splits;
-                uint32_t fix_phase = 0;
-                bool fix_ok = true;
+                // This was the CTA's last unit, so its operand ring (and the
+                // output staging) is idle.  Each warp streams its own 16 KB
+                // region of every other segment's partial (the sums of the
+                // rows and columns it holds) through three 8 KB slots of
+                // shared memory by asynchronous bulk copies, half a region at
+                // a time, and adds each half from shared memory as it lands;
+                // the warps do not wait for one another, and up to 192 KB are
+                // in flight per CTA.
                 // Integer sums may be added in any order.  Floating-point sums
                 // are added in segment order, this CTA's own from its slot as
                 // well, so the result does not depend on which segment
@@ -599,45 +615,64 @@ __global__ void __launch_bounds__(gemm_threads(kMode), 1)
 #pragma unroll
                     for (int i = 0; i < 128; ++i) acc[i] = 0;
                 }
-                for (int unit = first; unit < first + p.splits && fix_ok; ++unit) {
-                    if (!kFp32Sums && unit == u.slot) continue;
-                    const int4* other = p.partials + (static_cast<int64_t>(unit) * kPair + rank) * kPartialInt4;
-                    if (e == 0 && lane == 0) {
-                        fence_proxy_async_global();
-                        mbar_arrive_expect_tx(fixbar, kPartialInt4 * 16);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            bulk_load(smem + c * 16384, reinterpret_cast<const uint8_t*>(other) + c * 16384, 16384,
-                                      fixbar);
-                        s_fix_status = mbar_wait(fixbar, fix_phase, limit) ? 1 : 2;
+                const int first = (u.tile - p.dp_tiles) * p.splits;
+                const int n_units = kFp32Sums ? p.splits : p.splits - 1;
+                const int n_pieces = 2 * n_units;
+                uint8_t* wbuf = smem + e * kFixWarpBytes;
+                uint64_t* wbar = fixbars + e * kFixSlots;
+                auto piece_src = [&](int j) -> const uint8_t* {
+                    int unit = first + (j >> 1);
+                    if (!kFp32Sums && unit >= u.slot) ++unit;   // this segment's own partial is in registers
+                    const int4* region =
+                        p.partials + (static_cast<int64_t>(unit) * kPair + rank) * kPartialInt4 + e * 1024;
+                    return reinterpret_cast<const uint8_t*>(region) + (j & 1) * kFixSlotBytes;
+                };
+                if (lane == 0) {
+                    fence_proxy_async_global();
+                    for (int j = 0; j < kFixSlots && j < n_pieces; ++j) {
+                        mbar_arrive_expect_tx(&wbar[j], kFixSlotBytes);
+                        bulk_load(wbuf + j * kFixSlotBytes, piece_src(j), kFixSlotBytes, &wbar[j]);
                     }
-                    epi_barrier();
-                    fix_ok = (s_fix_status == 1);
-                    if (fix_ok) {
-                        const int4* sp = reinterpret_cast<const int4*>(smem) + e * 32 * 32 + lane;
+                }
+                bool fix_ok = true;
+                for (int k = 0; k < n_units && fix_ok; ++k) {
 #pragma unroll
-                        for (int g = 0; g < 32; ++g) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int j = 2 * k + hh;
+                        const int slot = j % kFixSlots;
+                        const bool landed = mbar_wait(&wbar[slot], static_cast<uint32_t>(j / kFixSlots) & 1u, limit);
+                        if (!__all_sync(0xFFFFFFFFu, landed)) {
+                            fix_ok = false;
+                            break;
+                        }
+                        const int4* sp = reinterpret_cast<const int4*>(wbuf + slot * kFixSlotBytes) + lane;
+#pragma unroll
+                        for (int g = 0; g < 16; ++g) {
                             const int4 v = sp[g * 32];
+                            const int a = 4 * (16 * hh + g);
                             if constexpr (kFp32Sums) {
-                                acc[4 * g] = __float_as_int(__fadd_rn(__int_as_float(acc[4 * g]), __int_as_float(v.x)));
-                                acc[4 * g + 1] =
-                                    __float_as_int(__fadd_rn(__int_as_float(acc[4 * g + 1]), __int_as_float(v.y)));
-                                acc[4 * g + 2] =
-                                    __float_as_int(__fadd_rn(__int_as_float(acc[4 * g + 2]), __int_as_float(v.z)));
-                                acc[4 * g + 3] =
-                                    __float_as_int(__fadd_rn(__int_as_float(acc[4 * g + 3]), __int_as_float(v.w)));
+                                acc[a] = __float_as_int(__fadd_rn(__int_as_float(acc[a]), __int_as_float(v.x)));
+                                acc[a + 1] = __float_as_int(__fadd_rn(__int_as_float(acc[a + 1]), __int_as_float(v.y)));
+                                acc[a + 2] = __float_as_int(__fadd_rn(__int_as_float(acc[a + 2]), __int_as_float(v.z)));
+                                acc[a + 3] = __float_as_int(__fadd_rn(__int_as_float(acc[a + 3]), __int_as_float(v.w)));
                             } else {
-                                acc[4 * g] += v.x;
-                                acc[4 * g + 1] += v.y;
-                                acc[4 * g + 2] += v.z;
-                                acc[4 * g + 3] += v.w;
+                                acc[a] += v.x;
+                                acc[a + 1] += v.y;
+                                acc[a + 2] += v.z;
+                                acc[a + 3] += v.w;
                             }
                         }
+                        __syncwarp();   // every lane has read the slot before it is refilled
+                        if (lane == 0 && j + kFixSlots < n_pieces) {
+                            mbar_arrive_expect_tx(&wbar[slot], kFixSlotBytes);
+                            bulk_load(wbuf + slot * kFixSlotBytes, piece_src(j + kFixSlots), kFixSlotBytes,
+                                      &wbar[slot]);
+                        }
                     }
-                    epi_barrier();   // everyone has read it before the next copy lands
-                    fix_phase ^= 1u;
                 }
-                if (!fix_ok) {
+                if (!fix_ok && lane == 0) s_fix_status = 1;
+                epi_barrier();
+                if (s_fix_status != 0) {
                     if (e == 0 && lane == 0) atomicOr(p.status, kDevTimeoutEpilogue);
                     ok = false;
                     break;
