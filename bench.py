@@ -79,7 +79,7 @@ def gemm_bytes(M, N, K, bias_size=2, code_size=1):
 GEMM_SOURCES = ["w8a8_int8_linear_act_b300/csrc/gemm_tcgen05.cuh",
                 "w8a8_int8_linear_act_b300/csrc/ptx_sm103.cuh"]
 GEMM_TRAFFIC = {"4c6119a28db36d2a": 164.14e6, "fd3b36ebdcdd6b15": 167.30e6, "7b406bc72ed21ced": 167.26e6,
-                "25c25b09727d8201": 168.16e6, "523c87070454c4cf": 165.93e6}
+                "25c25b09727d8201": 168.16e6, "523c87070454c4cf": 165.93e6, "6bc2643ac23e769c": 167.38e6}
 
 
 def sources_digest(paths):

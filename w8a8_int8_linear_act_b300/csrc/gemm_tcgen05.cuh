@@ -664,6 +664,7 @@ __global__ void __launch_bounds__(gemm_threads(kMode), 1)
                         }
                         __syncwarp();   // every lane has read the slot before it is refilled
                         if (lane == 0 && j + kFixSlots < n_pieces) {
+                            fence_proxy_async_smem();   // those reads before the copy's writes
                             mbar_arrive_expect_tx(&wbar[slot], kFixSlotBytes);
                             bulk_load(wbuf + slot * kFixSlotBytes, piece_src(j + kFixSlots), kFixSlotBytes,
                                       &wbar[slot]);
