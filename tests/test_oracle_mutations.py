@@ -68,6 +68,14 @@ def _epilogue_mutant(kind):
             n = min(len(sx), len(sw))
             return real(acc, np.resize(sw, len(sx)).astype(np.float32), np.resize(sx, len(sw)).astype(np.float32),
                         bias) if n else real(acc, sx, sw, bias)
+        if kind == "scales_first":
+            # acc * (sx * sw): the two scales multiplied first, in fp32
+            acc = np.asarray(acc)
+            s2 = (np.asarray(sx, np.float32)[:, None] * np.asarray(sw, np.float32)[None, :]).astype(np.float32)
+            y32 = (acc.astype(np.float32) * s2).astype(np.float32)
+            if bias is not None:
+                y32 = (y32 + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+            return y32, oracle.bf16_rne(y32)
         return real(acc, sx, sw, bias)
     return e
 
@@ -129,7 +137,8 @@ GEMM_PINS = [pins.test_gemm_k1_all_code_pairs_brute_force, pins.test_gemm_hand_e
              pins.test_gemm_matches_numpy_int64_matmul, pins.test_gemm_int32_limit,
              pins.test_gemm_f64_path_equals_scalar_path_large_sums]
 EPI_PINS = [pins.test_epilogue_zero_acc_gives_bias, pins.test_epilogue_exact_powers_of_two,
-            pins.test_epilogue_indices_against_float64, pins.test_linear_zero_row_outputs_bias]
+            pins.test_epilogue_indices_against_float64, pins.test_linear_zero_row_outputs_bias,
+            pins.test_epilogue_rounding_order]
 BF16_PINS = [pins.test_bf16_linear_brute_force, pins.test_bf16_linear_identity_and_roles,
              pins.test_bf16_linear_closed_form_and_tolerance]
 QK_PINS = [pins.test_qk_blocks_brute_force, pins.test_qk_blocks_layouts_agree, pins.test_qk_blocks_special_block_sizes,
@@ -148,6 +157,7 @@ MUTANTS = [
     ("gemm_s32_f64", "last k term dropped", _gemm_mutant("drop_last_k"), GEMM_PINS),
     ("epilogue", "bias dropped", _epilogue_mutant("no_bias"), EPI_PINS),
     ("epilogue", "row and column scales swapped", _epilogue_mutant("scales_swapped"), EPI_PINS),
+    ("epilogue", "scales multiplied together first", _epilogue_mutant("scales_first"), EPI_PINS),
     ("bf16_linear_f64", "bias dropped", _bf16_linear_mutant("no_bias"), BF16_PINS),
     ("bf16_linear_f64", "W not transposed", _bf16_linear_mutant("w_not_transposed"), BF16_PINS),
     ("quantize_qk_blocks", "block one token too long", _qk_mutant("block_off_by_one"), QK_PINS),

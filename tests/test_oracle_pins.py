@@ -300,6 +300,34 @@ def test_epilogue_indices_against_float64():
     assert (np.abs(yf - y32) <= oracle.ulp_bf16(y32) / 2).all()
 
 
+def test_epilogue_rounding_order():
+    """The dequantisation takes its fp32 roundings in the stated order:
+    (float)acc * sx, then * sw, then + bias, each rounded once (zhidx
+    TurboT2VA article, section 01 item 3: scale and bias once after the full
+    INT32 sum; the order is this build's reading of it).  The expected values
+    are computed here in exact binary64 arithmetic: every product of an
+    integer below 2^21 or an fp32 value with an fp32 value, and every sum of
+    two fp32 values of these sizes, is exact in binary64, so converting each
+    step to float32 rounds it once, to nearest even.  About a third of these
+    random triples give a different fp32 result when sx * sw is formed first,
+    so the test tells the orders apart."""
+    rng = np.random.default_rng(77)
+    acc = rng.integers(-2 ** 20, 2 ** 20, size=(16, 24)).astype(np.int32)
+    sx = rng.uniform(1e-3, 1.0, 16).astype(np.float32)
+    sw = rng.uniform(1e-4, 1e-2, 24).astype(np.float32)
+    b = rng.uniform(-1, 1, 24).astype(np.float32)
+    y32, _ = oracle.epilogue(acc, sx, sw, b)
+    a64 = acc.astype(np.float64)
+    step1 = (a64 * sx[:, None].astype(np.float64)).astype(np.float32)
+    step2 = (step1.astype(np.float64) * sw[None, :].astype(np.float64)).astype(np.float32)
+    expect = (step2.astype(np.float64) + b[None, :].astype(np.float64)).astype(np.float32)
+    assert np.array_equal(y32, expect)
+    s2 = (sx[:, None].astype(np.float64) * sw[None, :].astype(np.float64)).astype(np.float32)
+    other = ((a64 * s2.astype(np.float64)).astype(np.float32).astype(np.float64)
+             + b[None, :].astype(np.float64)).astype(np.float32)
+    assert (other != expect).mean() > 0.1
+
+
 # --------------------------------------------------------------------------
 # Whole path
 # --------------------------------------------------------------------------
